@@ -1,0 +1,162 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention (KDA) hot path.
+ *
+ * KDA is a gated delta rule whose forget gate decays each KEY CHANNEL separately
+ * (the "per-K-channel exp2(gk)" decay of vllm.cpp PR #110 "chunk_kda prefill AOT
+ * port", commit description; vllm.cpp PR #122 "fold Kimi-Linear onto the shared
+ * paged runner", block B2, contrasts it with GDN's per-head decay).  For one head
+ * with state S (K x V, row = key channel) and token t:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * The library has the two halves of the prefill=chunk / decode=recurrent split
+ * (PR #110 commit description; PR #113 "paged-incremental decode", commit body):
+ *
+ *   kda_chunk_prefill     -- the whole prompt of each packed sequence, chunk by
+ *                            chunk (64 tokens), from an optional initial state;
+ *                            returns the outputs and the final state per sequence
+ *                            (the state carried into decode, PR #113).
+ *   kda_recurrent_decode  -- one token per sequence against the state held in a
+ *                            paged pool slot, updated in place (state slots keyed
+ *                            by per-sequence indices, PR #122 block B2).
+ *
+ * Conventions for every call
+ * --------------------------
+ *  * Pointers are DEVICE pointers (cudaMalloc / torch CUDA memory) unless stated;
+ *    each must be 16-byte aligned.  All tensors are dense and row-major with the
+ *    last dimension contiguous:
+ *        q, k, g : [tokens, H, K]     v, out : [tokens, H, V]     beta : [tokens, H]
+ *        states  : [.., H, K, V]      (V fastest; a state row is one key channel)
+ *  * dtype (KDA_DTYPE_*) is the element type of q, k and v; out_dtype that of out
+ *    (either may be fp32 or bf16; an fp32 out suits an fp32 residual stream, and a
+ *    bf16 out holds exactly the fp32 result rounded to nearest).  g, beta and all
+ *    states are fp32.  g is the NATURAL-log gate (g <= 0 for a decay); the kernels
+ *    work in exp2 space internally.  Accumulation is fp32.
+ *  * The caller owns every buffer.  The library allocates no device or host memory,
+ *    keeps no per-call state, and synchronises nothing: all work is enqueued on
+ *    `stream` (a cudaStream_t; NULL = the legacy default stream).  Errors from the
+ *    kernels themselves surface at the caller's next synchronisation.
+ *  * Return value: KDA_OK (0) or a negative kda_status; on error nothing has been
+ *    enqueued.  kda_status_string() names a status.
+ *  * Aliasing: no output may overlap an input byte range, except that the prefill's
+ *    final_state may be EXACTLY init_state (in-place carry).  Violations give
+ *    KDA_ERR_ALIAS (the byte-range guard idea of flare PR #23, "Kimi K3: fused
+ *    decode pack and retained-buffer compaction", design notes).
+ *  * Supported shapes: K, V in {64, 128}; H >= 1.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+/* Element type of q, k, v (dtype) and of out (out_dtype). */
+enum kda_dtype {
+    KDA_DTYPE_F32 = 0,
+    KDA_DTYPE_BF16 = 1
+};
+
+enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = -1,   /* null required pointer, negative size, misaligned pointer,
+                                   non-finite scale */
+    KDA_ERR_UNSUPPORTED = -2,   /* K or V outside {64, 128}, unknown dtype or out_dtype */
+    KDA_ERR_ALIAS = -3,         /* an output overlaps an input */
+    KDA_ERR_CUDA = -4           /* a CUDA runtime call or launch failed (see kda_last_cuda_error) */
+};
+
+/* KDA_ABI_VERSION of the loaded library. */
+KDA_API int kda_abi_version(void);
+
+/* Static, NUL-terminated name of a status code. */
+KDA_API const char *kda_status_string(int status);
+
+/* cudaError_t of the last failing CUDA call in this thread (0 if none). */
+KDA_API int kda_last_cuda_error(void);
+
+/*
+ * Chunked prefill over packed variable-length sequences.
+ *
+ * Defined by the chunked prompt path of vllm.cpp PR #110 (commit description: the
+ * in-chunk gate cumsum in exp2 space, the decayed intra-chunk k.k^T, the unit
+ * lower-triangular solve, the w/u recompute, the inter-chunk state propagation and
+ * the output), with the state carry of PR #113 (commit body: the final recurrent
+ * state of the prompt is the state the decode continues from).
+ *
+ *   q, k         [total_tokens, H, K]  dtype     queries / keys (callers normally
+ *                                                 L2-normalise them; not done here)
+ *   v            [total_tokens, H, V]  dtype     values
+ *   g            [total_tokens, H, K]  fp32      natural-log gate per key channel
+ *   beta         [total_tokens, H]     fp32      delta-rule write strength
+ *   scale                               fp32     output scale (e.g. 1/sqrt(K))
+ *   init_state   [num_seqs, H, K, V]   fp32      initial state per sequence, or NULL
+ *                                                 for zeros
+ *   cu_seqlens   [num_seqs + 1]        int32     sequence n is tokens
+ *                                                 [cu_seqlens[n], cu_seqlens[n+1]);
+ *                                                 read on the device.  Bounds are
+ *                                                 clamped to [0, total_tokens] and a
+ *                                                 decreasing pair is an empty sequence,
+ *                                                 so no access leaves the buffers.
+ *   out          [total_tokens, H, V]  out_dtype written for every token of every
+ *                                                 sequence; rows outside all sequences
+ *                                                 are not written
+ *   final_state  [num_seqs, H, K, V]   fp32      state after the last token of each
+ *                                                 sequence (init_state, or zeros, for an
+ *                                                 empty one), or NULL to skip.  May be
+ *                                                 exactly init_state.
+ *   total_tokens, num_seqs >= 0; H >= 1; K, V in {64, 128}; dtype, out_dtype kda_dtypes.
+ */
+KDA_API int kda_chunk_prefill(const void *q, const void *k, const void *v,
+                              const float *g, const float *beta, float scale,
+                              const float *init_state, const int32_t *cu_seqlens,
+                              void *out, float *final_state,
+                              int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
+                              int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                              int32_t out_dtype, void *stream);
+
+/*
+ * One recurrent decode step for num_seqs sequences with paged states.
+ *
+ * Defined by the decode side of the split: one token per sequence advanced from
+ * the carried state (vllm.cpp PR #113, commit body), over the paged state group
+ * whose slots are selected per sequence (vllm.cpp PR #122, block B2: state
+ * gather / scatter keyed by the per-sequence state indices).  Gather, update and
+ * scatter are one pass: each selected state is read once and written once.
+ *
+ *   q, k         [num_seqs, H, K]  dtype
+ *   v            [num_seqs, H, V]  dtype
+ *   g            [num_seqs, H, K]  fp32   natural-log gate
+ *   beta         [num_seqs, H]     fp32
+ *   state_pool   [num_slots, H, K, V] fp32  updated IN PLACE at the selected slots;
+ *                                           every other slot is left bit-identical
+ *   state_idx    [num_seqs]        int32  slot of each sequence, read on the device.
+ *                                           Slots must be distinct (duplicates race).
+ *                                           An index outside [0, num_slots) touches
+ *                                           no slot and gives zero outputs.
+ *   out          [num_seqs, H, V]  out_dtype
+ */
+KDA_API int kda_recurrent_decode(const void *q, const void *k, const void *v,
+                                 const float *g, const float *beta, float scale,
+                                 float *state_pool, const int32_t *state_idx, void *out,
+                                 int32_t num_seqs, int32_t num_slots, int32_t num_heads,
+                                 int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                                 int32_t out_dtype, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,152 @@
+"""ctypes binding of the in-tree ``libkda.so`` (the C ABI of ``include/kda.h``).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library.  There is no fallback of any kind; if the library is missing or fails to
+load, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = -1
+KDA_ERR_UNSUPPORTED = -2
+KDA_ERR_ALIAS = -3
+KDA_ERR_CUDA = -4
+KDA_DTYPE_F32 = 0
+KDA_DTYPE_BF16 = 1
+ABI_VERSION = 1
+
+EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
+            "kda_chunk_prefill", "kda_recurrent_decode")
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status}){detail}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is not built; run `python -m kimi_delta_attention_09_gb300.build` "
+            "(the KDA ops have no non-CUDA implementation)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, f32, i32, i64 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int32, ctypes.c_int64
+    lib.kda_abi_version.argtypes = []
+    lib.kda_abi_version.restype = ctypes.c_int
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_last_cuda_error.argtypes = []
+    lib.kda_last_cuda_error.restype = ctypes.c_int
+    lib.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
+                                      i64, i32, i32, i32, i32, i32, i32, vp]
+    lib.kda_chunk_prefill.restype = ctypes.c_int
+    lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp,
+                                         i32, i32, i32, i32, i32, i32, i32, vp]
+    lib.kda_recurrent_decode.restype = ctypes.c_int
+    if lib.kda_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"libkda.so ABI {lib.kda_abi_version()} != expected {ABI_VERSION}")
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.kda_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != KDA_OK:
+        detail = f", cudaError {lib.kda_last_cuda_error()}" if status == KDA_ERR_CUDA else ""
+        raise KdaError(fn, status, detail)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return KDA_DTYPE_F32
+    raise ValueError(f"unsupported dtype {t.dtype} (bf16 or fp32)")
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def kda_chunk_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
+                      stream=None) -> None:
+    """Enqueue ``kda_chunk_prefill`` on ``stream`` (default: torch's current stream).
+
+    Tensors are CUDA tensors laid out as include/kda.h states; shapes and dtypes are
+    read from them: q [T, H, K], v [T, H, V], cu_seqlens [N + 1] int32; the dtype of
+    ``out`` (fp32 or bf16) selects the output element type.
+    """
+    T, H, K = q.shape
+    V = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out),
+                    ("cu_seqlens", cu_seqlens), ("init_state", init_state),
+                    ("final_state", final_state)):
+        if t is not None:
+            _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _need(k.shape == q.shape and g.shape == q.shape, "q, k, g must be [T, H, K]")
+    _need(v.shape[:2] == (T, H) and out.shape == v.shape, "v, out must be [T, H, V]")
+    _need(beta.shape == (T, H), "beta must be [T, H]")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v must share one dtype")
+    import torch
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g, beta must be fp32")
+    _need(cu_seqlens.dtype == torch.int32, "cu_seqlens must be int32")
+    for s in (init_state, final_state):
+        if s is not None:
+            _need(s.dtype == torch.float32 and tuple(s.shape) == (N, H, K, V),
+                  "states must be fp32 [N, H, K, V]")
+    rc = lib.kda_chunk_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                               _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                               T, N, H, K, V, _dtype_code(q), _dtype_code(out),
+                               _stream_handle(stream))
+    _check("kda_chunk_prefill", rc)
+
+
+def kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out,
+                         stream=None) -> None:
+    """Enqueue ``kda_recurrent_decode``: q [N, H, K], v [N, H, V], pool [S, H, K, V]."""
+    N, H, K = q.shape
+    V = v.shape[-1]
+    S = state_pool.shape[0]
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out),
+                    ("state_pool", state_pool), ("state_idx", state_idx)):
+        _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    import torch
+    _need(k.shape == q.shape and g.shape == q.shape, "q, k, g must be [N, H, K]")
+    _need(v.shape[:2] == (N, H) and out.shape == v.shape, "v, out must be [N, H, V]")
+    _need(beta.shape == (N, H), "beta must be [N, H]")
+    _need(tuple(state_pool.shape[1:]) == (H, K, V) and state_pool.dtype == torch.float32,
+          "state_pool must be fp32 [S, H, K, V]")
+    _need(state_idx.dtype == torch.int32 and state_idx.numel() == N, "state_idx must be int32 [N]")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v must share one dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g, beta must be fp32")
+    rc = lib.kda_recurrent_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                  _ptr(state_pool), _ptr(state_idx), _ptr(out),
+                                  N, S, H, K, V, _dtype_code(q), _dtype_code(out),
+                                  _stream_handle(stream))
+    _check("kda_recurrent_decode", rc)

@@ -1,0 +1,147 @@
+// kda_api.cu -- the C ABI of include/kda.h: argument validation, the byte-range
+// alias guard and kernel selection.  No allocation, no synchronisation.
+#include <cmath>
+#include <cstdint>
+
+#include "kda.h"
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+    const void *p;
+    uint64_t bytes;
+};
+
+// [p, p + bytes) and [q, q + bytes) share at least one byte
+bool overlaps(const Range &a, const Range &b)
+{
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), a1 = a0 + a.bytes;
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b.p), b1 = b0 + b.bytes;
+    return a0 < b1 && b0 < a1;
+}
+
+bool dims_supported(int32_t d) { return d == 64 || d == 128; }
+bool dtype_supported(int32_t d) { return d == KDA_DTYPE_F32 || d == KDA_DTYPE_BF16; }
+
+int finish(cudaError_t e)
+{
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char *kda_status_string(int status)
+{
+    switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+int kda_last_cuda_error(void) { return g_last_cuda_error; }
+
+int kda_chunk_prefill(const void *q, const void *k, const void *v,
+                      const float *g, const float *beta, float scale,
+                      const float *init_state, const int32_t *cu_seqlens,
+                      void *out, float *final_state,
+                      int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
+                      int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                      int32_t out_dtype, void *stream)
+{
+    if (total_tokens < 0 || num_seqs < 0 || num_heads < 1 || !std::isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (!dtype_supported(dtype) || !dtype_supported(out_dtype)) return KDA_ERR_UNSUPPORTED;
+    if (!dims_supported(head_dim_k) || !dims_supported(head_dim_v)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KDA_OK;
+    if (!cu_seqlens || !aligned16(cu_seqlens)) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0) {
+        const void *req[] = {q, k, v, g, beta, out};
+        for (const void *p : req)
+            if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    }
+    if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
+        return KDA_ERR_INVALID_ARG;
+
+    const uint64_t T = (uint64_t)total_tokens, H = (uint64_t)num_heads;
+    const uint64_t K = (uint64_t)head_dim_k, V = (uint64_t)head_dim_v;
+    const uint64_t es = dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const uint64_t eo = out_dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const uint64_t state_bytes = (uint64_t)num_seqs * H * K * V * 4;
+    const Range in[] = {{q, T * H * K * es}, {k, T * H * K * es}, {v, T * H * V * es},
+                        {g, T * H * K * 4}, {beta, T * H * 4},
+                        {cu_seqlens, ((uint64_t)num_seqs + 1) * 4}};
+    const Range r_out{out, T * H * V * eo}, r_init{init_state, state_bytes},
+        r_final{final_state, state_bytes};
+    for (const Range &r : in)
+        if (overlaps(r_out, r) || overlaps(r_final, r)) return KDA_ERR_ALIAS;
+    if (overlaps(r_out, r_init) || overlaps(r_out, r_final)) return KDA_ERR_ALIAS;
+    if (overlaps(r_final, r_init) && final_state != init_state) return KDA_ERR_ALIAS;
+
+    kda::PrefillArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
+    a.init_state = init_state; a.cu_seqlens = cu_seqlens; a.out = out;
+    a.final_state = final_state; a.total_tokens = total_tokens; a.num_seqs = num_seqs;
+    a.num_heads = num_heads; a.head_dim_k = head_dim_k; a.head_dim_v = head_dim_v;
+    a.dtype = dtype; a.out_dtype = out_dtype;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return finish(kda::prefill_tc_supported(a) ? kda::launch_prefill_tc(a, st)
+                                               : kda::launch_prefill_simt(a, st));
+}
+
+int kda_recurrent_decode(const void *q, const void *k, const void *v,
+                         const float *g, const float *beta, float scale,
+                         float *state_pool, const int32_t *state_idx, void *out,
+                         int32_t num_seqs, int32_t num_slots, int32_t num_heads,
+                         int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                         int32_t out_dtype, void *stream)
+{
+    if (num_seqs < 0 || num_slots < 0 || num_heads < 1 || !std::isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (!dtype_supported(dtype) || !dtype_supported(out_dtype)) return KDA_ERR_UNSUPPORTED;
+    if (!dims_supported(head_dim_k) || !dims_supported(head_dim_v)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KDA_OK;
+    const void *req[] = {q, k, v, g, beta, state_idx, out};
+    for (const void *p : req)
+        if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    if (num_slots > 0 && (!state_pool || !aligned16(state_pool))) return KDA_ERR_INVALID_ARG;
+
+    const uint64_t N = (uint64_t)num_seqs, H = (uint64_t)num_heads;
+    const uint64_t K = (uint64_t)head_dim_k, V = (uint64_t)head_dim_v;
+    const uint64_t es = dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const uint64_t eo = out_dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const Range in[] = {{q, N * H * K * es}, {k, N * H * K * es}, {v, N * H * V * es},
+                        {g, N * H * K * 4}, {beta, N * H * 4}, {state_idx, N * 4}};
+    const Range r_out{out, N * H * V * eo};
+    const Range r_pool{state_pool, (uint64_t)num_slots * H * K * V * 4};
+    for (const Range &r : in)
+        if (overlaps(r_out, r) || overlaps(r_pool, r)) return KDA_ERR_ALIAS;
+    if (overlaps(r_out, r_pool)) return KDA_ERR_ALIAS;
+
+    kda::DecodeArgs a;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
+    a.pool = state_pool; a.state_idx = state_idx; a.out = out;
+    a.num_seqs = num_seqs; a.num_slots = num_slots; a.num_heads = num_heads;
+    a.head_dim_k = head_dim_k; a.head_dim_v = head_dim_v; a.dtype = dtype;
+    a.out_dtype = out_dtype;
+    return finish(kda::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

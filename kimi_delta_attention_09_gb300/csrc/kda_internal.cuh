@@ -1,0 +1,66 @@
+// kda_internal.cuh -- internal declarations shared by the KDA CUDA sources.
+// Not part of the public ABI (include/kda.h is).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// One prefill call, already validated by the C-ABI layer.
+struct PrefillArgs {
+    const void *q, *k, *v;        // [T, H, K] / [T, H, V], dtype
+    const float *g, *beta;        // [T, H, K] fp32, [T, H] fp32
+    float scale;
+    const float *init_state;      // [N, H, K, V] or nullptr
+    const int32_t *cu_seqlens;    // [N + 1]
+    void *out;                    // [T, H, V], out_dtype
+    float *final_state;           // [N, H, K, V] or nullptr
+    int64_t total_tokens;
+    int32_t num_seqs, num_heads, head_dim_k, head_dim_v, dtype, out_dtype;
+};
+
+// One decode step, already validated by the C-ABI layer.
+struct DecodeArgs {
+    const void *q, *k, *v;        // [N, H, K] / [N, H, V], dtype
+    const float *g, *beta;        // [N, H, K], [N, H]
+    float scale;
+    float *pool;                  // [S, H, K, V]
+    const int32_t *state_idx;     // [N]
+    void *out;                    // [N, H, V], out_dtype
+    int32_t num_seqs, num_slots, num_heads, head_dim_k, head_dim_v, dtype, out_dtype;
+};
+
+constexpr int kDtypeF32 = 0;
+constexpr int kDtypeBF16 = 1;
+constexpr int kChunk = 64;              // tokens per prefill chunk
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Chunked prefill on CUDA cores in fp32 (any supported dtype / head size).
+cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t stream);
+// Chunked prefill on tensor cores (bf16 q/k/v with K = V = 128).
+bool prefill_tc_supported(const PrefillArgs &a);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
+// One-token paged decode.
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Clamp a device-read sequence range to [0, total] (an inverted pair is empty).
+__device__ __forceinline__ void clamp_range(int64_t total, int32_t b, int32_t e,
+                                            int64_t &bos, int64_t &eos) {
+    bos = b < 0 ? 0 : (b > total ? total : b);
+    eos = e < 0 ? 0 : (e > total ? total : e);
+    if (eos < bos) eos = bos;
+}
+
+}  // namespace kda

@@ -1,0 +1,148 @@
+"""The C ABI without a GPU: the library loads, exports what include/kda.h declares,
+the header compiles as C, and argument validation / the alias guard reject bad calls
+before anything is enqueued (no CUDA call is made on these paths)."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def native():
+    from kimi_delta_attention_09_gb300 import build
+    build.build()
+    from kimi_delta_attention_09_gb300 import _native
+    return _native
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    assert "kda_chunk_prefill" in syms and "kda_recurrent_decode" in syms
+    assert len(syms) >= 5
+
+
+def test_library_exports_every_declared_symbol(native):
+    out = subprocess.run(["nm", "-D", "--defined-only", native.LIB_PATH], check=True,
+                         capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(kda_\w+)", out))
+    for s in declared_symbols():
+        assert s in exported, s
+        assert hasattr(native.lib, s)
+    assert set(native.EXPORTED) == set(declared_symbols())
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "kda.h"\nint main(void) { return kda_abi_version() == '
+                   'KDA_ABI_VERSION ? KDA_OK : KDA_ERR_CUDA; }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I" + os.path.dirname(HEADER), "-c", str(src), "-o",
+                    str(tmp_path / "use.o")], check=True)
+
+
+def test_status_strings(native):
+    assert native.lib.kda_abi_version() == 1
+    for code, name in [(0, "KDA_OK"), (-1, "KDA_ERR_INVALID_ARG"), (-2, "KDA_ERR_UNSUPPORTED"),
+                       (-3, "KDA_ERR_ALIAS"), (-4, "KDA_ERR_CUDA")]:
+        assert native.status_string(code) == name
+    assert native.status_string(7) == "KDA_ERR_UNKNOWN"
+
+
+# Fake, never-dereferenced device addresses: validation must decide from the
+# addresses and sizes alone.  Every call below is built to FAIL validation (or to
+# have nothing to do), so no kernel is ever launched on these addresses.
+BASE = 1 << 40
+
+
+def _prefill(native, **kw):
+    T, N, H, K, V, es = kw.get("T", 100), kw.get("N", 2), 2, 64, 64, 2
+    a = dict(q=BASE, k=BASE + (1 << 24), v=BASE + (2 << 24), g=BASE + (3 << 24),
+             beta=BASE + (4 << 24), scale=0.125, init=BASE + (5 << 24), cu=BASE + (6 << 24),
+             out=BASE + (7 << 24), final=BASE + (8 << 24), T=T, N=N, H=H, K=K, V=V, dtype=1,
+             out_dtype=1)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return native.lib.kda_chunk_prefill(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
+        vp(a["init"]), vp(a["cu"]), vp(a["out"]), vp(a["final"]), a["T"], a["N"], a["H"],
+        a["K"], a["V"], a["dtype"], a["out_dtype"], None)
+
+
+def _decode(native, **kw):
+    a = dict(q=BASE, k=BASE + (1 << 24), v=BASE + (2 << 24), g=BASE + (3 << 24),
+             beta=BASE + (4 << 24), scale=0.125, pool=BASE + (1 << 32), idx=BASE + (6 << 24),
+             out=BASE + (7 << 24), N=4, S=8, H=2, K=128, V=128, dtype=1, out_dtype=1)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return native.lib.kda_recurrent_decode(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
+        vp(a["pool"]), vp(a["idx"]), vp(a["out"]), a["N"], a["S"], a["H"], a["K"], a["V"],
+        a["dtype"], a["out_dtype"], None)
+
+
+def test_prefill_argument_validation(native):
+    assert _prefill(native, q=None) == native.KDA_ERR_INVALID_ARG
+    assert _prefill(native, cu=None) == native.KDA_ERR_INVALID_ARG
+    assert _prefill(native, out=BASE + (7 << 24) + 8) == native.KDA_ERR_INVALID_ARG  # misaligned
+    assert _prefill(native, T=-1) == native.KDA_ERR_INVALID_ARG
+    assert _prefill(native, H=0) == native.KDA_ERR_INVALID_ARG
+    assert _prefill(native, scale=float("nan")) == native.KDA_ERR_INVALID_ARG
+    assert _prefill(native, K=96) == native.KDA_ERR_UNSUPPORTED
+    assert _prefill(native, V=256) == native.KDA_ERR_UNSUPPORTED
+    assert _prefill(native, dtype=5) == native.KDA_ERR_UNSUPPORTED
+    assert _prefill(native, out_dtype=2) == native.KDA_ERR_UNSUPPORTED
+    assert _prefill(native, N=0) == native.KDA_OK            # nothing to do, nothing enqueued
+
+
+def test_prefill_alias_guard(native):
+    # out overlapping q, v, g, beta or cu_seqlens
+    for key in ("q", "v", "g", "beta", "cu"):
+        base = {"q": BASE, "v": BASE + (2 << 24), "g": BASE + (3 << 24),
+                "beta": BASE + (4 << 24), "cu": BASE + (6 << 24)}[key]
+        assert _prefill(native, out=base) == native.KDA_ERR_ALIAS, key
+    # an fp32 out is twice as long as a bf16 one: 2 bytes past the bf16 end of out
+    # would be free for bf16 but overlaps for fp32 (out is [100, 2, 64])
+    bf16_end = BASE + (9 << 24)
+    assert _prefill(native, out=bf16_end - 100 * 2 * 64 * 4 + 16, final=bf16_end,
+                    out_dtype=0) == native.KDA_ERR_ALIAS
+    # final_state overlapping k (partial overlap, not just equal start)
+    assert _prefill(native, final=BASE + (1 << 24) + 4096) == native.KDA_ERR_ALIAS
+    # final_state partially overlapping init_state is rejected ...
+    assert _prefill(native, final=BASE + (5 << 24) + 16) == native.KDA_ERR_ALIAS
+    # ... out overlapping final_state is rejected ...
+    assert _prefill(native, out=BASE + (8 << 24) + 64) == native.KDA_ERR_ALIAS
+
+
+def test_decode_argument_validation_and_alias(native):
+    assert _decode(native, idx=None) == native.KDA_ERR_INVALID_ARG
+    assert _decode(native, pool=None) == native.KDA_ERR_INVALID_ARG
+    assert _decode(native, K=32) == native.KDA_ERR_UNSUPPORTED
+    assert _decode(native, N=-1) == native.KDA_ERR_INVALID_ARG
+    assert _decode(native, N=0) == native.KDA_OK
+    # out inside the pool, pool overlapping an input
+    assert _decode(native, out=BASE + (1 << 32) + 4096) == native.KDA_ERR_ALIAS
+    assert _decode(native, pool=BASE + (3 << 24)) == native.KDA_ERR_ALIAS
+    assert _decode(native, idx=BASE + (1 << 32) + 64) == native.KDA_ERR_ALIAS
+
+
+def test_binding_refuses_missing_library(tmp_path, monkeypatch):
+    """No fallback: the binding raises when libkda.so is absent."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "kda_native_copy", os.path.join(ROOT, "kimi_delta_attention_09_gb300", "_native.py"))
+    mod = importlib.util.module_from_spec(spec)
+    monkeypatch.setattr(os.path, "exists",
+                        lambda p, _e=os.path.exists: False if p.endswith("libkda.so") else _e(p))
+    with pytest.raises(RuntimeError, match="not built"):
+        spec.loader.exec_module(mod)

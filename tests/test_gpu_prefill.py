@@ -1,0 +1,155 @@
+"""Chunked prefill on the GPU against the fp64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kimi_delta_attention_09_gb300 import inputs
+from _helpers import TOL, cuda, dtype_name, oracle_prefill, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def run_prefill(case, init_in_place=False, final=True, out_dtype=torch.float32):
+    """Run the GPU prefill.  Parity is judged on fp32 outputs (the arithmetic error
+    alone); a bf16 output is checked separately to be that fp32 result rounded."""
+    from kimi_delta_attention_09_gb300 import _native
+    q, k, v, g, beta = (cuda(x) for x in (case.q, case.k, case.v, case.g, case.beta))
+    cu = cuda(case.cu_seqlens)
+    init = cuda(case.init_state)
+    out = torch.full(v.shape, float("nan"), dtype=out_dtype, device="cuda")
+    fin = None
+    if final:
+        fin = init if (init_in_place and init is not None) else torch.full(
+            (case.N, case.H, case.K, case.V), float("nan"), device="cuda")
+    _native.kda_chunk_prefill(q, k, v, g, beta, case.scale, init, cu, out, fin)
+    torch.cuda.synchronize()
+    return out.cpu(), (None if fin is None else fin.cpu())
+
+
+def check_case(case, heads=None, seqs=None, **kw):
+    out, fin = run_prefill(case, **kw)
+    heads = list(range(case.H)) if heads is None else heads
+    seqs = list(range(case.N)) if seqs is None else seqs
+    ref_out, ref_fin = oracle_prefill(case, heads, seqs)
+    tol = TOL[dtype_name(case.q)]
+    rows = np.concatenate([np.arange(int(case.cu_seqlens[n]), int(case.cu_seqlens[n + 1]))
+                           for n in seqs]) if seqs else np.zeros(0, dtype=np.int64)
+    e_out = rel_err(out[rows][:, heads], ref_out[rows]) if rows.size else 0.0
+    e_fin = rel_err(fin[seqs][:, heads], ref_fin)
+    assert e_out <= tol, f"out rel err {e_out:.3e} > {tol}"
+    assert e_fin <= tol, f"final state rel err {e_fin:.3e} > {tol}"
+    return e_out, e_fin
+
+
+def test_tiny_f32_workload():
+    """B=1, H=2, T=128, K=V=64, fp32 -- the oracle-sized case, full comparison."""
+    check_case(inputs.tiny_f32())
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("K,V", [(128, 128), (64, 64), (128, 64), (64, 128)])
+def test_ragged_varlen_with_initial_state(dtype, K, V):
+    """Several chunks, ragged tails (1, 63, 64, 65, 200 tokens), nonzero init."""
+    case = inputs.prefill_case([1, 63, 64, 65, 200], H=3, K=K, V=V, dtype=dtype,
+                               seed=60 + K + V, init_std=0.02)
+    check_case(case)
+
+
+def test_final_state_in_place_and_empty_sequences():
+    """final_state == init_state carries in place; empty sequences return init."""
+    case = inputs.prefill_case([0, 130, 0, 5], H=2, K=128, V=128, dtype="bf16", seed=61,
+                               init_std=0.05)
+    check_case(case, init_in_place=True)
+    out, fin = run_prefill(case)
+    assert torch.equal(fin[0], case.init_state[0]) and torch.equal(fin[2], case.init_state[2])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_bf16_output_is_the_rounded_fp32_output(dtype):
+    """out_dtype=bf16 stores exactly round-to-nearest(bf16) of the fp32 result."""
+    case = inputs.prefill_case([1, 64, 130], H=2, K=128, V=128, dtype=dtype, seed=66,
+                               init_std=0.02)
+    o32, f32 = run_prefill(case, out_dtype=torch.float32)
+    o16, f16 = run_prefill(case, out_dtype=torch.bfloat16)
+    assert torch.equal(o16.view(torch.int16), o32.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(f16, f32)
+
+
+def test_zero_init_and_no_final_state():
+    case = inputs.prefill_case([97], H=2, K=128, V=128, dtype="bf16", seed=62)
+    out, fin = run_prefill(case, final=False)
+    ref, _ = oracle_prefill(case)
+    assert fin is None and rel_err(out, ref) <= TOL["bf16"]
+
+
+def test_split_prefill_carries_state():
+    """Prefill [0, T1) then [T1, T) from the returned state = prefill of [0, T)."""
+    full = inputs.prefill_case([300], H=2, K=128, V=128, dtype="bf16", seed=63, init_std=0.02)
+    T1 = 137
+    a = inputs.PrefillCase(name="a", seed=0, q=full.q[:T1], k=full.k[:T1], v=full.v[:T1],
+                           g=full.g[:T1], beta=full.beta[:T1],
+                           cu_seqlens=torch.tensor([0, T1], dtype=torch.int32),
+                           init_state=full.init_state, scale=full.scale)
+    out_a, fin_a = run_prefill(a)
+    b = inputs.PrefillCase(name="b", seed=0, q=full.q[T1:], k=full.k[T1:], v=full.v[T1:],
+                           g=full.g[T1:], beta=full.beta[T1:],
+                           cu_seqlens=torch.tensor([0, 300 - T1], dtype=torch.int32),
+                           init_state=fin_a, scale=full.scale)
+    out_b, fin_b = run_prefill(b)
+    ref_out, ref_fin = oracle_prefill(full)
+    assert rel_err(torch.cat([out_a, out_b]), ref_out) <= TOL["bf16"]
+    assert rel_err(fin_b, ref_fin) <= TOL["bf16"]
+
+
+def test_strong_gates():
+    """Gates down to -5 per step per channel (a naive exp factorisation overflows)."""
+    case = inputs.prefill_case([150], H=2, K=128, V=128, dtype="bf16", seed=64)
+    gen = torch.Generator().manual_seed(64)
+    case.g = (-5.0 * torch.rand(case.g.shape, generator=gen)).float()
+    check_case(case)
+
+
+def test_prefill_then_decode_matches_full_recurrence():
+    """Prompt through the chunked prefill, state scattered into a pool slot, then
+    token-by-token decode = the oracle over the whole sequence."""
+    from kimi_delta_attention_09_gb300 import _native
+    T0, steps, H = 200, 6, 2
+    full = inputs.prefill_case([T0 + steps], H=H, K=128, V=128, dtype="bf16", seed=65)
+    pre = inputs.PrefillCase(name="p", seed=0, q=full.q[:T0], k=full.k[:T0], v=full.v[:T0],
+                             g=full.g[:T0], beta=full.beta[:T0],
+                             cu_seqlens=torch.tensor([0, T0], dtype=torch.int32),
+                             init_state=None, scale=full.scale)
+    out_p, fin_p = run_prefill(pre)
+    pool = torch.zeros(3, H, 128, 128, device="cuda")
+    pool[1] = fin_p[0].cuda()
+    idx = torch.tensor([1], dtype=torch.int32, device="cuda")
+    outs = []
+    for t in range(T0, T0 + steps):
+        o = torch.empty(1, H, 128, dtype=torch.float32, device="cuda")
+        sl = slice(t, t + 1)
+        _native.kda_recurrent_decode(cuda(full.q[sl]), cuda(full.k[sl]), cuda(full.v[sl]),
+                                     cuda(full.g[sl]), cuda(full.beta[sl]), full.scale, pool,
+                                     idx, o)
+        outs.append(o.cpu())
+    ref_out, ref_fin = oracle_prefill(full)
+    assert rel_err(torch.cat([out_p] + outs), ref_out) <= TOL["bf16"]
+    assert rel_err(pool[1].cpu(), ref_fin[0]) <= TOL["bf16"]
+
+
+# ------------------------------------------------------------ full-size workloads
+
+def test_single_prompt_workload_sampled_heads():
+    """B=1, H=32, T=4096, K=V=128 bf16: all outputs and states of 4 sampled heads."""
+    check_case(inputs.single_prompt(), heads=[0, 9, 22, 31])
+
+
+def test_varlen_packed_workload_sampled():
+    """8 packed sequences (lengths 256..8192), nonzero init: 3 sequences x 3 heads."""
+    case = inputs.varlen_packed()
+    check_case(case, heads=[1, 16, 30], seqs=[0, 4, 6])
+
+
+def test_long_prefill_workload_sampled():
+    """B=1, H=32, T=65536: 2 sampled heads, every output and the final state."""
+    check_case(inputs.long_prefill(), heads=[5, 27])
