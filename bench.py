@@ -72,13 +72,18 @@ def load_peaks():
 
 
 def load_traffic():
-    """Per-launch DRAM bytes from the committed ncu summaries (or None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """Per-launch DRAM bytes recorded from ncu captures in profiles/traffic.txt."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    out = {}
     try:
         with open(path) as f:
-            return json.load(f)
-    except Exception:
-        return {}
+            for line in f:
+                parts = line.split("#", 1)[0].split()
+                if len(parts) == 2:
+                    out[parts[0]] = None if parts[1] == "null" else int(parts[1])
+    except OSError:
+        pass
+    return out
 
 
 class ClockSampler:

@@ -36,7 +36,11 @@
 // mirrored to shared memory in fp16 as the next chunk's MMA operand.  The raw
 // inputs of chunk j+1 are fetched with cp.async while chunk j's solve and state
 // step run.
+#include <cstring>
+
+#include <cuda.h>
 #include <cuda_fp16.h>
+#include <cudaTypedefs.h>
 
 #include "kda_internal.cuh"
 
@@ -71,7 +75,7 @@ struct Smem {
     static constexpr int tm = kh + C * LD128 * 2;            // f16  T  [64][LD64]
     static constexpr int aqk = tm + C * LD64 * 2;            // f16  A_qk [64][LD64]
     static constexpr int ht = aqk + C * LD64 * 2;            // f16  h^T [32][LD128]
-    static constexpr int xt = ht + VT * LD128 * 2;           // f16  (beta X)^T [32][LD64]; T-solve scratch
+    static constexpr int xt = ht + VT * LD128 * 2;           // f16  (beta X)^T [32][LD64]; xt+dt hold fp16 A_kk in the solve
     static constexpr int dt = xt + VT * LD64 * 2;            // f16  D^T [32][LD64]
     static constexpr int vs = dt + VT * LD64 * 2;            // f32  V [64][LDV]
     static constexpr int beta = vs + C * LDV * 4;            // f32  [64]
@@ -81,11 +85,12 @@ struct Smem {
     static constexpr int fm = pm + 4 * KD * 4;               // f32  [4][128] 2^(G_last - m_R)
     static constexpr int rho = fm + 4 * KD * 4;              // f16  [6][128] 2^(m_R - m_I), I < R
     static constexpr int flag = rho + 6 * KD * 2;            // int
-    static constexpr int total = flag + 16;
+    static constexpr int mbar = flag + 8;                    // u64 mbarrier of the chunk loads
+    static constexpr int total = mbar + 8;
 };
 static_assert(Smem::total <= 232448, "shared memory budget");
 static_assert(C * LDA * 4 <= C * LD128 * 2, "A_kk must fit in the a_k region");
-static_assert(3 * 256 * 4 <= VT * LD64 * 2, "T-solve scratch must fit in xt");
+static_assert(Smem::dt == Smem::xt + VT * LD64 * 2 && 2 * VT == C, "fp16 A_kk spans xt and dt");
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -107,12 +112,6 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1)
-{
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];\n"
-                 : "=r"(r0), "=r"(r1) : "r"(addr));
-}
-
 // D += A * B, m16n8k16, fp16 operands, fp32 accumulators
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1)
@@ -124,12 +123,6 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n"
-                 :: "r"(dst), "l"(src), "r"(src_bytes));
-}
-
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, int src_bytes)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n"
@@ -137,6 +130,47 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, int src
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+
+// 3-D tiled TMA load (tensor map in kernel-parameter space) completing on an mbarrier
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t mbar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];\n"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(mbar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" :: "r"(mbar), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+                 :: "r"(mbar), "r"(bytes) : "memory");
+}
+
+// Bounded wait for the phase with parity `parity` to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
+{
+    for (int i = 0; i < (1 << 22); ++i) {
+        uint32_t done;
+        asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                     "selp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all()
 {
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
@@ -171,46 +205,53 @@ __device__ __forceinline__ int bkn_off(int lane, int k0, int n0, int ld)
     return (k0 + (lane & 7) + (((lane >> 3) & 1) << 3)) * ld + n0 + ((lane >> 4) << 3);
 }
 
+// Tensor maps of q, k, g (box 128 channels x 1 head x 64 tokens) and v (box 32
+// columns x 1 head x 64 tokens), built on the host for each call.
+struct TmaMaps {
+    CUtensorMap q, k, g, v;
+};
+
 // ------------------------------------------------------------------ loads
+// Tokens [t0, t0+64) of q, k, g and of this CTA's 32 v columns arrive as four TMA
+// tiles that complete on the chunk mbarrier (rows past the end of the tensor are
+// zero-filled by the TMA unit; rows past the end of the SEQUENCE are zeroed after
+// arrival, see zero_tail_rows).  beta (strided by H) uses 4-byte cp.async.  Called
+// by all threads after a barrier that ends every read of the raw buffers.
 __device__ __forceinline__ void issue_chunk_loads(unsigned char *sm, const PrefillArgs &a,
-                                                  int64_t t0, int len, int h, int vt, int tid)
+                                                  const TmaMaps &maps, int64_t t0, int len,
+                                                  int h, int vt, int tid)
 {
-    const int H = a.num_heads;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-    // q, k: 64 rows x 256 B = 16 x 16 B pieces per row
-    for (int p = tid; p < C * 16; p += kThreads) {
-        const int r = p >> 4, piece = p & 15;
-        const int valid = r < len;
-        const int64_t row = t0 + (valid ? r : 0);
-        const int64_t off = (row * H + h) * KD + piece * 8;
-        cp_async16(smem_u32(sm + Smem::q_raw + (r * KD + piece * 8) * 2), q + off, valid ? 16 : 0);
-        cp_async16(smem_u32(sm + Smem::k_raw + (r * KD + piece * 8) * 2), k + off, valid ? 16 : 0);
-    }
-    // g: 64 rows x 512 B = 32 pieces per row
-    for (int p = tid; p < C * 32; p += kThreads) {
-        const int r = p >> 5, piece = p & 31;
-        const int valid = r < len;
-        const int64_t row = t0 + (valid ? r : 0);
-        cp_async16(smem_u32(sm + Smem::g_raw + (r * KD + piece * 4) * 4),
-                   a.g + (row * H + h) * KD + piece * 4, valid ? 16 : 0);
-    }
-    // v tile: 64 rows x 64 B = 4 pieces per row
-    {
-        const int r = tid >> 2, piece = tid & 3;   // exactly 256 pieces
-        const int valid = r < len;
-        const int64_t row = t0 + (valid ? r : 0);
-        cp_async16(smem_u32(sm + Smem::v_raw + (r * VT + piece * 8) * 2),
-                   v + (row * H + h) * VD + vt * VT + piece * 8, valid ? 16 : 0);
-    }
-    // beta: 64 scalars with stride H
     if (tid < C) {
         const int valid = tid < len;
         const int64_t row = t0 + (valid ? tid : 0);
-        cp_async4(smem_u32(sm + Smem::b_raw + tid * 4), a.beta + row * H + h, valid ? 4 : 0);
+        cp_async4(smem_u32(sm + Smem::b_raw + tid * 4), a.beta + row * a.num_heads + h, valid ? 4 : 0);
     }
     cp_async_commit();
+    if (tid == 0) {
+        const uint32_t mbar = smem_u32(sm + Smem::mbar);
+        fence_proxy_async_smem();   // earlier generic reads of the raw buffers come first
+        mbar_arrive_expect_tx(mbar, C * (2 * KD * 2 + KD * 4 + VT * 2));
+        const int z = (int)t0;
+        tma_load_3d(smem_u32(sm + Smem::q_raw), &maps.q, 0, h, z, mbar);
+        tma_load_3d(smem_u32(sm + Smem::k_raw), &maps.k, 0, h, z, mbar);
+        tma_load_3d(smem_u32(sm + Smem::g_raw), &maps.g, 0, h, z, mbar);
+        tma_load_3d(smem_u32(sm + Smem::v_raw), &maps.v, vt * VT, h, z, mbar);
+    }
+}
+
+// Zero the rows [len, 64) of the raw tiles (tokens of the next sequence).
+__device__ __forceinline__ void zero_tail_rows(unsigned char *sm, int len, int tid)
+{
+    for (int e = tid; e < (C - len) * KD / 8; e += kThreads) {   // 16 B per store
+        const int r = len + e / (KD / 8), piece = e % (KD / 8);
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(sm + Smem::q_raw + (r * KD + piece * 8) * 2) = z;
+        *reinterpret_cast<uint4 *>(sm + Smem::k_raw + (r * KD + piece * 8) * 2) = z;
+        *reinterpret_cast<uint4 *>(sm + Smem::g_raw + (r * KD + piece * 8) * 4) = z;
+        *reinterpret_cast<uint4 *>(sm + Smem::g_raw + (r * KD + piece * 8 + 4) * 4) = z;
+        if (piece < VT / 8)
+            *reinterpret_cast<uint4 *>(sm + Smem::v_raw + (r * VT + piece * 8) * 2) = z;
+    }
 }
 
 // Exact-exponential intra-chunk matrices for chunks outside the fp16 factor range:
@@ -256,7 +297,7 @@ __device__ void exact_intra_chunk(unsigned char *sm, int tid)
 
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
-kda_prefill_tc_kernel(PrefillArgs a)
+kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
 {
     extern __shared__ __align__(128) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -291,7 +332,6 @@ kda_prefill_tc_kernel(PrefillArgs a)
     __half *rho = reinterpret_cast<__half *>(sm + Smem::rho);
     volatile int *flag = reinterpret_cast<volatile int *>(sm + Smem::flag);
     float *akk = reinterpret_cast<float *>(sm + Smem::a_k);       // aliases a_k after P3
-    float *scratch = reinterpret_cast<float *>(sm + Smem::xt);    // T-solve scratch
 
     int64_t bos, eos;
     clamp_range(a.total_tokens, a.cu_seqlens[n], a.cu_seqlens[n + 1], bos, eos);
@@ -320,29 +360,46 @@ kda_prefill_tc_kernel(PrefillArgs a)
         *reinterpret_cast<uint32_t *>(ht + (v0 + 8) * LD128 + c) = pack_h2(hreg[nt][2], hreg[nt][3]);
     }
 
-    if (bos < eos) issue_chunk_loads(sm, a, bos, (int)((eos - bos) < C ? (eos - bos) : C), h, vt, tid);
+    const uint32_t mbar = smem_u32(sm + Smem::mbar);
+    if (tid == 0) mbar_init(mbar, 1);
+    __syncthreads();
+    if (bos < eos) issue_chunk_loads(sm, a, maps, bos, (int)((eos - bos) < C ? (eos - bos) : C), h, vt, tid);
 
     Tout *out = static_cast<Tout *>(a.out);
+    uint32_t load_parity = 0;
+    bool failed = false;
 
     for (int64_t t0 = bos; t0 < eos; t0 += C) {
         const int len = (int)((eos - t0) < C ? (eos - t0) : C);
         cp_async_wait_all();
+        if (!mbar_wait(mbar, load_parity)) {
+            // the chunk's copies did not land within the wait bound: stop, and mark
+            // this CTA's outputs as invalid (NaN) below instead of hanging
+            failed = true;
+        }
+        load_parity ^= 1u;
+        if (!failed && len < C) zero_tail_rows(sm, len, tid);
+        if (__syncthreads_or(failed)) { failed = true; break; }
         if (tid == 0) *flag = 0;
-        __syncthreads();
 
         // ---------------- P1: in-chunk gate cumsum, exp2 space (two halves of 32 rows)
         {
             const int c = tid & 127, half = tid >> 7;
             float acc = 0.f;
-            for (int r = 32 * half; r < 32 * half + 32; ++r) {
-                acc += G[r * KD + c] * kLog2e;
-                G[r * KD + c] = acc;
+#pragma unroll
+            for (int r0 = 32 * half; r0 < 32 * half + 32; r0 += 8) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = G[(r0 + u) * KD + c];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) { acc += x[u] * kLog2e; G[(r0 + u) * KD + c] = acc; }
             }
         }
         __syncthreads();
         if (tid >= 128) {
             const int c = tid & 127;
             const float base = G[31 * KD + c];
+#pragma unroll 8
             for (int r = 32; r < 64; ++r) G[r * KD + c] += base;
         }
         __syncthreads();
@@ -373,33 +430,45 @@ kda_prefill_tc_kernel(PrefillArgs a)
         }
         __syncthreads();
 
-        // ---------------- P2: factors and fp16 operands, two channels per thread
+        // ---------------- P2: factors and fp16 operands, four channels per thread
         {
             bool bad = false;
-            for (int e = tid; e < C * KD / 2; e += kThreads) {
-                const int r = e >> 6, c = (e & 63) * 2, R = r >> 4;
-                float ok[2], oq[2], ob[2], ot[2], oqt[2], okh[2];
+#pragma unroll 2
+            for (int e = tid; e < C * KD / 4; e += kThreads) {
+                const int r = e >> 5, c = (e & 31) * 4, R = r >> 4;
+                const float4 gv = *reinterpret_cast<const float4 *>(G + r * KD + c);
+                const float4 mv = *reinterpret_cast<const float4 *>(mref + R * KD + c);
+                const float4 pv = *reinterpret_cast<const float4 *>(pm + R * KD + c);
+                const float4 fv = *reinterpret_cast<const float4 *>(fm + R * KD + c);
+                const uint2 kb = *reinterpret_cast<const uint2 *>(kraw + r * KD + c);
+                const uint2 qb = *reinterpret_cast<const uint2 *>(qraw + r * KD + c);
+                const float g4[4] = {gv.x, gv.y, gv.z, gv.w}, m4[4] = {mv.x, mv.y, mv.z, mv.w};
+                const float p4[4] = {pv.x, pv.y, pv.z, pv.w}, f4[4] = {fv.x, fv.y, fv.z, fv.w};
+                const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kb.x));
+                const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kb.y));
+                const float2 q01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qb.x));
+                const float2 q23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qb.y));
+                const float k4[4] = {k01.x, k01.y, k23.x, k23.y}, q4[4] = {q01.x, q01.y, q23.x, q23.y};
+                float ok[4], oq[4], ob[4], ot[4], oqt[4], okh[4];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const float x = G[r * KD + c + u] - mref[R * KD + c + u];
+                for (int u = 0; u < 4; ++u) {
+                    const float x = g4[u] - m4[u];
                     const float em = exp2f(x), ep = exp2f(-x);
                     bad |= !(em <= kFactorMax && ep <= kFactorMax);
-                    const float kv = __bfloat162float(kraw[r * KD + c + u]);
-                    const float qv = __bfloat162float(qraw[r * KD + c + u]);
-                    ok[u] = kv * em;
-                    oq[u] = qv * em;
-                    ob[u] = kv * ep;
-                    ot[u] = -ok[u] * pm[R * KD + c + u];
-                    oqt[u] = oq[u] * pm[R * KD + c + u];
-                    okh[u] = ob[u] * fm[R * KD + c + u];
+                    ok[u] = k4[u] * em;
+                    oq[u] = q4[u] * em;
+                    ob[u] = k4[u] * ep;
+                    ot[u] = -ok[u] * p4[u];
+                    oqt[u] = oq[u] * p4[u];
+                    okh[u] = ob[u] * f4[u];
                 }
                 const int o = r * LD128 + c;
-                *reinterpret_cast<uint32_t *>(ak + o) = pack_h2(ok[0], ok[1]);
-                *reinterpret_cast<uint32_t *>(aq + o) = pack_h2(oq[0], oq[1]);
-                *reinterpret_cast<uint32_t *>(bk + o) = pack_h2(ob[0], ob[1]);
-                *reinterpret_cast<uint32_t *>(nkt + o) = pack_h2(ot[0], ot[1]);
-                *reinterpret_cast<uint32_t *>(qt + o) = pack_h2(oqt[0], oqt[1]);
-                *reinterpret_cast<uint32_t *>(kh + o) = pack_h2(okh[0], okh[1]);
+                *reinterpret_cast<uint2 *>(ak + o) = make_uint2(pack_h2(ok[0], ok[1]), pack_h2(ok[2], ok[3]));
+                *reinterpret_cast<uint2 *>(aq + o) = make_uint2(pack_h2(oq[0], oq[1]), pack_h2(oq[2], oq[3]));
+                *reinterpret_cast<uint2 *>(bk + o) = make_uint2(pack_h2(ob[0], ob[1]), pack_h2(ob[2], ob[3]));
+                *reinterpret_cast<uint2 *>(nkt + o) = make_uint2(pack_h2(ot[0], ot[1]), pack_h2(ot[2], ot[3]));
+                *reinterpret_cast<uint2 *>(qt + o) = make_uint2(pack_h2(oqt[0], oqt[1]), pack_h2(oqt[2], oqt[3]));
+                *reinterpret_cast<uint2 *>(kh + o) = make_uint2(pack_h2(okh[0], okh[1]), pack_h2(okh[2], okh[3]));
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) *flag = 1;
         }
@@ -408,49 +477,73 @@ kda_prefill_tc_kernel(PrefillArgs a)
 
         // ---------------- P3: A_kk and A_qk (lower block triangle) on tensor cores
         if (!exact_path) {
-            float acc[5][4];
+            // warp -> (matrix, row block R, up to three 16-column blocks I <= R); the A
+            // fragments of a row block are loaded once per k-step and reused.
+            const int mat = warp >> 2, sub = warp & 3;
+            const __half *A = mat == 0 ? ak : aq;
+            // (R, I) of this warp's column blocks; sub 3 also takes row block 0
+            const int nblk = sub == 2 ? 3 : 2 + (sub == 3);
+            int Rb[3], Ib[3];
+            if (sub == 0)      { Rb[0] = 3; Ib[0] = 0; Rb[1] = 3; Ib[1] = 1; Rb[2] = 3; Ib[2] = 1; }
+            else if (sub == 1) { Rb[0] = 3; Ib[0] = 2; Rb[1] = 3; Ib[1] = 3; Rb[2] = 3; Ib[2] = 3; }
+            else if (sub == 2) { Rb[0] = 2; Ib[0] = 0; Rb[1] = 2; Ib[1] = 1; Rb[2] = 2; Ib[2] = 2; }
+            else               { Rb[0] = 1; Ib[0] = 0; Rb[1] = 1; Ib[1] = 1; Rb[2] = 0; Ib[2] = 0; }
+            float acc[3][2][4];
 #pragma unroll
-            for (int j = 0; j < 5; ++j) {
-                const int t = warp + 8 * j;                 // 40 tiles: (matrix, R, n8-tile)
-                const int mat = t / 20, rem = t % 20;
-                const int R = rem < 2 ? 0 : rem < 6 ? 1 : rem < 12 ? 2 : 3;
-                const int nt = rem - (R == 0 ? 0 : R == 1 ? 2 : R == 2 ? 6 : 12);
-                const int I = nt >> 1;
-                const __half *A = mat == 0 ? ak : aq;
-                acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-                const int pair = I < R ? R * (R - 1) / 2 + I : -1;
+            for (int b = 0; b < 3; ++b)
 #pragma unroll
-                for (int ks = 0; ks < KD / 16; ++ks) {
-                    uint32_t af[4], b0, b1;
-                    ldsm_x4(smem_u32(A + a_off(lane, 16 * R, 16 * ks, LD128)), af[0], af[1], af[2], af[3]);
-                    ldsm_x2(smem_u32(bk + (8 * nt + (lane & 7)) * LD128 + 16 * ks + (((lane >> 3) & 1) << 3)),
-                            b0, b1);
-                    if (pair >= 0) {
-                        const __half *rp = rho + pair * KD + 16 * ks + 2 * tig;
-                        b0 = hmul2_u32(b0, *reinterpret_cast<const uint32_t *>(rp));
-                        b1 = hmul2_u32(b1, *reinterpret_cast<const uint32_t *>(rp + 8));
+                for (int t = 0; t < 2; ++t) acc[b][t][0] = acc[b][t][1] = acc[b][t][2] = acc[b][t][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KD / 16; ++ks) {
+                uint32_t afr[2][4];
+                ldsm_x4(smem_u32(A + a_off(lane, 16 * Rb[0], 16 * ks, LD128)),
+                        afr[0][0], afr[0][1], afr[0][2], afr[0][3]);
+                if (sub == 3)
+                    ldsm_x4(smem_u32(A + a_off(lane, 0, 16 * ks, LD128)),
+                            afr[1][0], afr[1][1], afr[1][2], afr[1][3]);
+#pragma unroll
+                for (int b = 0; b < 3; ++b) {
+                    if (b < nblk) {
+                        const int R = Rb[b], I = Ib[b];
+                        uint32_t bf[4];
+                        ldsm_x4(smem_u32(bk + bnk_off(lane, 16 * I, 16 * ks, LD128)),
+                                bf[0], bf[1], bf[2], bf[3]);
+                        if (I < R) {
+                            const int pair = R * (R - 1) / 2 + I;
+                            const __half *rp = rho + pair * KD + 16 * ks + 2 * tig;
+                            const uint32_t s0 = *reinterpret_cast<const uint32_t *>(rp);
+                            const uint32_t s1 = *reinterpret_cast<const uint32_t *>(rp + 8);
+                            bf[0] = hmul2_u32(bf[0], s0); bf[1] = hmul2_u32(bf[1], s1);
+                            bf[2] = hmul2_u32(bf[2], s0); bf[3] = hmul2_u32(bf[3], s1);
+                        }
+                        const bool alt = (sub == 3 && b == 2);   // row block 0 of warp sub 3
+                        const uint32_t af[4] = {alt ? afr[1][0] : afr[0][0], alt ? afr[1][1] : afr[0][1],
+                                                alt ? afr[1][2] : afr[0][2], alt ? afr[1][3] : afr[0][3]};
+                        mma16816(acc[b][0], af, bf[0], bf[1]);
+                        mma16816(acc[b][1], af, bf[2], bf[3]);
                     }
-                    mma16816(acc[j], af, b0, b1);
                 }
             }
             __syncthreads();   // every read of a_k / a_q / b_k is done; a_k becomes A_kk (fp32)
 #pragma unroll
-            for (int j = 0; j < 5; ++j) {
-                const int t = warp + 8 * j;
-                const int mat = t / 20, rem = t % 20;
-                const int R = rem < 2 ? 0 : rem < 6 ? 1 : rem < 12 ? 2 : 3;
-                const int nt = rem - (R == 0 ? 0 : R == 1 ? 2 : R == 2 ? 6 : 12);
+            for (int b = 0; b < 3; ++b) {
+                if (b < nblk) {
+                    const int R = Rb[b], I = Ib[b];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int r = 16 * R + g8 + 8 * hh;
-                    const int i = 8 * nt + 2 * tig;
-                    const float v0 = acc[j][2 * hh], v1 = acc[j][2 * hh + 1];
-                    if (mat == 0) {
-                        akk[r * LDA + i] = (i < r) ? beta_s[r] * v0 : 0.f;
-                        akk[r * LDA + i + 1] = (i + 1 < r) ? beta_s[r] * v1 : 0.f;
-                    } else {
-                        *reinterpret_cast<uint32_t *>(aqk + r * LD64 + i) =
-                            pack_h2(i <= r ? v0 : 0.f, i + 1 <= r ? v1 : 0.f);
+                    for (int t = 0; t < 2; ++t) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int r = 16 * R + g8 + 8 * hh;
+                            const int i = 16 * I + 8 * t + 2 * tig;
+                            const float v0 = acc[b][t][2 * hh], v1 = acc[b][t][2 * hh + 1];
+                            if (mat == 0) {
+                                akk[r * LDA + i] = (i < r) ? beta_s[r] * v0 : 0.f;
+                                akk[r * LDA + i + 1] = (i + 1 < r) ? beta_s[r] * v1 : 0.f;
+                            } else {
+                                *reinterpret_cast<uint32_t *>(aqk + r * LD64 + i) =
+                                    pack_h2(i <= r ? v0 : 0.f, i + 1 <= r ? v1 : 0.f);
+                            }
+                        }
                     }
                 }
             }
@@ -462,67 +555,78 @@ kda_prefill_tc_kernel(PrefillArgs a)
         // raw buffers are free: fetch the next chunk while the solve and state step run
         if (t0 + C < eos) {
             const int64_t t1 = t0 + C;
-            issue_chunk_loads(sm, a, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, tid);
+            issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, tid);
         }
 
-        // ---------------- P4: T = (I + A_kk)^-1, blocked, fp32
-        if (warp < 4) {
-            // diagonal 16x16 block R = warp, forward substitution; lane j owns column j
-            const int R = warp, j = lane & 15;
-            float col[16];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) col[m] = (m == j) ? 1.f : 0.f;
-            const float *Ab = akk + (16 * R) * LDA + 16 * R;
-#pragma unroll
-            for (int r = 1; r < 16; ++r) {
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-                for (int m = 0; m < r; m += 2) {
-                    s0 += Ab[r * LDA + m] * col[m];
-                    if (m + 1 < r) s1 += Ab[r * LDA + m + 1] * col[m + 1];
-                }
-                if (j < r) col[r] = -(s0 + s1);
+        // ---------------- P4: T = (I + A_kk)^-1 in 16x16 blocks
+        // Diagonal blocks: fp32 forward substitution, one warp per block (lane j owns
+        // column j).  Below-diagonal blocks, by distance from the diagonal:
+        //     T_RI = -T_RR sum_{J=I}^{R-1} A_RJ T_JI
+        // on tensor cores, evaluated transposed (X^T = sum T_JI^T A_RJ^T, then
+        // T_RI^T = -X^T T_RR^T) so X^T passes from accumulator to operand in registers.
+        {
+            __half *akh = reinterpret_cast<__half *>(sm + Smem::xt);   // A_kk fp16 [64][LD64]
+            for (int e = tid; e < 6 * 128; e += kThreads) {            // 6 blocks x 16 rows x 8 pairs
+                const int blk = e >> 7, rem = e & 127, rr = rem >> 3, pp = (rem & 7) * 2;
+                const int R = blk == 0 ? 1 : blk < 3 ? 2 : 3;
+                const int J = blk - (R == 1 ? 0 : R == 2 ? 1 : 3);
+                const int r = 16 * R + rr, m = 16 * J + pp;
+                *reinterpret_cast<uint32_t *>(akh + r * LD64 + m) =
+                    pack_h2(akk[r * LDA + m], akk[r * LDA + m + 1]);
             }
-            __syncwarp();
-            if (lane < 16) {
+            if (warp < 4) {
+                const int R = warp, j = lane & 15;
+                float col[16];
 #pragma unroll
-                for (int r = 0; r < 16; ++r) akk[(16 * R + r) * LDA + 16 * R + j] = col[r];
-            }
-        }
-        __syncthreads();
-        for (int R = 1; R < 4; ++R) {
-            // X_I = sum_{J=I}^{R-1} A_RJ T_JI for I < R
-            for (int e = tid; e < R * 256; e += kThreads) {
-                const int I = e >> 8, rr = (e >> 4) & 15, ii = e & 15;
-                float s = 0.f;
-                for (int J = I; J < R; ++J) {
-                    const float *arow = akk + (16 * R + rr) * LDA + 16 * J;
-                    const float *tcol = akk + (16 * J) * LDA + 16 * I + ii;
+                for (int m = 0; m < 16; ++m) col[m] = (m == j) ? 1.f : 0.f;
+                const float *Ab = akk + (16 * R) * LDA + 16 * R;
 #pragma unroll
-                    for (int m = 0; m < 16; ++m) s += arow[m] * tcol[m * LDA];
+                for (int r = 1; r < 16; ++r) {
+                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int m = 0; m < r; ++m) s4[m & 3] += Ab[r * LDA + m] * col[m];
+                    if (j < r) col[r] = -((s4[0] + s4[1]) + (s4[2] + s4[3]));
                 }
-                scratch[e] = s;
+                if (lane < 16) {
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) tmh[(16 * R + r) * LD64 + 16 * R + j] = __float2half_rn(col[r]);
+                }
             }
             __syncthreads();
-            // T_RI = -T_RR X_I  (written over A_RI, which is no longer read)
-            for (int e = tid; e < R * 256; e += kThreads) {
-                const int I = e >> 8, rr = (e >> 4) & 15, ii = e & 15;
-                const float *trow = akk + (16 * R + rr) * LDA + 16 * R;
-                float s = 0.f;
+            for (int lvl = 1; lvl < 4; ++lvl) {
+                if (warp < 4 - lvl) {
+                    const int I = warp, R = warp + lvl;
+                    float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int J = I; J < R; ++J) {
+                        uint32_t af[4], bf[4];
+                        // A = T_JI^T (rows i, cols m) from T_JI stored [m][i]
+                        ldsm_x4_t(smem_u32(tmh + (16 * J + (lane & 7) + ((lane >> 4) << 3)) * LD64 +
+                                           16 * I + (((lane >> 3) & 1) << 3)),
+                                  af[0], af[1], af[2], af[3]);
+                        // B = A_RJ^T as [k=m][n=r] from A_RJ stored [r][m]
+                        ldsm_x4(smem_u32(akh + bnk_off(lane, 16 * R, 16 * J, LD64)), bf[0], bf[1], bf[2], bf[3]);
+                        mma16816(xa[0], af, bf[0], bf[1]);
+                        mma16816(xa[1], af, bf[2], bf[3]);
+                    }
+                    const uint32_t xf[4] = {pack_h2(-xa[0][0], -xa[0][1]), pack_h2(-xa[0][2], -xa[0][3]),
+                                            pack_h2(-xa[1][0], -xa[1][1]), pack_h2(-xa[1][2], -xa[1][3])};
+                    uint32_t tb[4];
+                    ldsm_x4(smem_u32(tmh + bnk_off(lane, 16 * R, 16 * R, LD64)), tb[0], tb[1], tb[2], tb[3]);
+                    float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    mma16816(ta[0], xf, tb[0], tb[1]);
+                    mma16816(ta[1], xf, tb[2], tb[3]);
 #pragma unroll
-                for (int p = 0; p < 16; ++p) s += trow[p] * scratch[(I << 8) + (p << 4) + ii];
-                akk[(16 * R + rr) * LDA + 16 * I + ii] = -s;
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 16 * I + g8 + ((e >> 1) << 3);
+                            const int r = 16 * R + 8 * nt + 2 * tig + (e & 1);
+                            tmh[r * LD64 + i] = __float2half_rn(ta[nt][e]);
+                        }
+                }
+                __syncthreads();
             }
-            __syncthreads();
         }
-        // T to fp16 (blocks on or below the diagonal; diagonal blocks carry their zeros)
-        for (int e = tid; e < C * C / 2; e += kThreads) {
-            const int r = e >> 5, i = (e & 31) * 2;
-            if (i < 16 * (r >> 4) + 16)
-                *reinterpret_cast<uint32_t *>(tmh + r * LD64 + i) =
-                    pack_h2(akk[r * LDA + i], akk[r * LDA + i + 1]);
-        }
-        __syncthreads();
 
         // ---------------- S1: X^T = V^T - h^T K~^T,  O1^T = h^T Q~^T   (rows v of mt, cols r of qw)
         float xacc[2][4], oacc[2][4];
@@ -624,6 +728,14 @@ kda_prefill_tc_kernel(PrefillArgs a)
         // the next iteration's first barrier orders these writes before their reads
     }
 
+    if (failed) {
+        // error marker: NaN state; the copies still in flight get one more bounded wait
+        mbar_wait(mbar, load_parity);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) hreg[nt][e] = __int_as_float(0x7fc00000);
+    }
     if (a.final_state) {
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
@@ -637,15 +749,54 @@ kda_prefill_tc_kernel(PrefillArgs a)
     }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess || q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// [T, H, inner] row-major tensor, box (box_inner x 1 x 64)
+bool encode_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int esize, int64_t T,
+                int H, int inner, int box_inner)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)inner * esize, (cuuint64_t)inner * esize * H};
+    const cuuint32_t box[3] = {(cuuint32_t)box_inner, 1u, (cuuint32_t)C};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, type, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename Tout>
 cudaError_t launch_tc_t(const PrefillArgs &a, cudaStream_t stream)
 {
+    TmaMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    const int H = a.num_heads;
+    if (a.total_tokens > 0) {   // with no tokens no tile is ever loaded
+        const int64_t T = a.total_tokens;
+        if (!encode_map(&maps.q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, KD, KD) ||
+            !encode_map(&maps.k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, KD, KD) ||
+            !encode_map(&maps.g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T, H, KD, KD) ||
+            !encode_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, VD, VT))
+            return cudaErrorInvalidValue;
+    }
     const int smem = Smem::total;
     cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel<Tout>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((int64_t)a.num_seqs * kVTiles), (unsigned)a.num_heads);
-    kda_prefill_tc_kernel<Tout><<<grid, kThreads, smem, stream>>>(a);
+    kda_prefill_tc_kernel<Tout><<<grid, kThreads, smem, stream>>>(a, maps);
     return cudaGetLastError();
 }
 
