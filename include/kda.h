@@ -17,6 +17,8 @@
  *                            chunk (64 tokens), from an optional initial state;
  *                            returns the outputs and the final state per sequence
  *                            (the state carried into decode, PR #113).
+ *   kda_chunk_prefill_paged -- the same prefill with the initial and final states in
+ *                            paged pool slots selected per sequence (in place).
  *   kda_recurrent_decode  -- one token per sequence against the state held in a
  *                            paged pool slot, updated in place (state slots keyed
  *                            by per-sequence indices, PR #122 block B2).
@@ -126,6 +128,33 @@ KDA_API int kda_chunk_prefill(const void *q, const void *k, const void *v,
                               int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
                               int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
                               int32_t out_dtype, void *stream);
+
+/*
+ * Chunked prefill whose per-sequence states live in paged pool slots.
+ *
+ * The prompt path over the paged state group (vllm.cpp PR #122 "fold Kimi-Linear
+ * onto the shared paged runner", block B2: the chunked prefill for fresh prompts
+ * and the state gather / scatter over the group's slots keyed by per-sequence state
+ * indices).  Same computation as kda_chunk_prefill, except that sequence n starts
+ * from the state held in slot state_idx[n] of state_pool and its final state is
+ * written back to that slot, in place.  A fresh prompt starts from a zeroed slot.
+ *
+ *   q, k, v, g, beta, scale, cu_seqlens, out   as for kda_chunk_prefill
+ *   state_pool   [num_slots, H, K, V]  fp32   read and updated IN PLACE at the selected
+ *                                              slots; every other slot is left bit-identical
+ *   state_idx    [num_seqs]            int32  slot of each sequence, read on the device.
+ *                                              Slots must be distinct (duplicates race).
+ *                                              An index outside [0, num_slots) reads and
+ *                                              writes no slot: that sequence runs from a
+ *                                              zero state and its final state is dropped.
+ */
+KDA_API int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
+                                    const float *g, const float *beta, float scale,
+                                    float *state_pool, const int32_t *state_idx,
+                                    const int32_t *cu_seqlens, void *out,
+                                    int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
+                                    int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+                                    int32_t dtype, int32_t out_dtype, void *stream);
 
 /*
  * One recurrent decode step for num_seqs sequences with paged states.

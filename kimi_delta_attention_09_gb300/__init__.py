@@ -9,11 +9,13 @@ pointers; importing the op functions raises if the library is missing.
 """
 from __future__ import annotations
 
-__all__ = ["chunk_prefill", "recurrent_decode", "kda_chunk_prefill", "kda_recurrent_decode"]
+__all__ = ["chunk_prefill", "chunk_prefill_paged", "recurrent_decode", "kda_chunk_prefill",
+           "kda_chunk_prefill_paged", "kda_recurrent_decode"]
 
 
 def __getattr__(name):
-    if name in ("kda_chunk_prefill", "kda_recurrent_decode", "KdaError"):
+    if name in ("kda_chunk_prefill", "kda_chunk_prefill_paged", "kda_recurrent_decode",
+                "KdaError"):
         from . import _native
         return getattr(_native, name)
     raise AttributeError(name)
@@ -42,6 +44,23 @@ def chunk_prefill(q, k, v, g, beta, scale=None, init_state=None, cu_seqlens=None
     _native.kda_chunk_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
                               final_state, stream)
     return out, final_state
+
+
+def chunk_prefill_paged(q, k, v, g, beta, state_pool, state_idx, scale=None, cu_seqlens=None,
+                        out_dtype=None, stream=None):
+    """Chunked prefill with each sequence's state in slot ``state_idx[n]`` of
+    ``state_pool`` (read as the initial state, overwritten with the final state)."""
+    import torch
+    from . import _native
+    T, H, K = q.shape
+    if scale is None:
+        scale = K ** -0.5
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=q.device)
+    out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
+    _native.kda_chunk_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens,
+                                    out, stream)
+    return out
 
 
 def recurrent_decode(q, k, v, g, beta, state_pool, state_idx, scale=None, out_dtype=None,

@@ -22,7 +22,7 @@ KDA_DTYPE_BF16 = 1
 ABI_VERSION = 1
 
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
-            "kda_chunk_prefill", "kda_recurrent_decode")
+            "kda_chunk_prefill", "kda_chunk_prefill_paged", "kda_recurrent_decode")
 
 
 class KdaError(RuntimeError):
@@ -47,6 +47,9 @@ def _load() -> ctypes.CDLL:
     lib.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
                                       i64, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_chunk_prefill.restype = ctypes.c_int
+    lib.kda_chunk_prefill_paged.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
+                                            i64, i32, i32, i32, i32, i32, i32, i32, vp]
+    lib.kda_chunk_prefill_paged.restype = ctypes.c_int
     lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp,
                                          i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_recurrent_decode.restype = ctypes.c_int
@@ -125,6 +128,35 @@ def kda_chunk_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out, fina
                                T, N, H, K, V, _dtype_code(q), _dtype_code(out),
                                _stream_handle(stream))
     _check("kda_chunk_prefill", rc)
+
+
+def kda_chunk_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens, out,
+                            stream=None) -> None:
+    """Enqueue ``kda_chunk_prefill_paged``: as ``kda_chunk_prefill`` with sequence n's
+    initial and final state in slot ``state_idx[n]`` of ``state_pool`` [S, H, K, V]."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    S = state_pool.shape[0]
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out),
+                    ("cu_seqlens", cu_seqlens), ("state_pool", state_pool),
+                    ("state_idx", state_idx)):
+        _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    import torch
+    _need(k.shape == q.shape and g.shape == q.shape, "q, k, g must be [T, H, K]")
+    _need(v.shape[:2] == (T, H) and out.shape == v.shape, "v, out must be [T, H, V]")
+    _need(beta.shape == (T, H), "beta must be [T, H]")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v must share one dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g, beta must be fp32")
+    _need(cu_seqlens.dtype == torch.int32, "cu_seqlens must be int32")
+    _need(tuple(state_pool.shape[1:]) == (H, K, V) and state_pool.dtype == torch.float32,
+          "state_pool must be fp32 [S, H, K, V]")
+    _need(state_idx.dtype == torch.int32 and state_idx.numel() == N, "state_idx must be int32 [N]")
+    rc = lib.kda_chunk_prefill_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                     _ptr(state_pool), _ptr(state_idx), _ptr(cu_seqlens),
+                                     _ptr(out), T, N, S, H, K, V, _dtype_code(q), _dtype_code(out),
+                                     _stream_handle(stream))
+    _check("kda_chunk_prefill_paged", rc)
 
 
 def kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out,

@@ -17,9 +17,32 @@ struct PrefillArgs {
     const int32_t *cu_seqlens;    // [N + 1]
     void *out;                    // [T, H, V], out_dtype
     float *final_state;           // [N, H, K, V] or nullptr
+    float *state_pool;            // [S, H, K, V] or nullptr: states live in slots state_idx[n]
+    const int32_t *state_idx;     // [N] (with state_pool)
+    int32_t num_slots;
     int64_t total_tokens;
     int32_t num_seqs, num_heads, head_dim_k, head_dim_v, dtype, out_dtype;
 };
+
+// Base pointers of the (sequence n, head h) state for a prefill: the caller's
+// init/final arrays, or slot state_idx[n] of the pool (nullptr for both when the
+// slot index is out of range, which makes the sequence start from zeros and drop
+// its final state).
+__device__ __forceinline__ void prefill_state_ptrs(const PrefillArgs &a, int64_t n, int h,
+                                                   const float *&init, float *&fin)
+{
+    const int64_t kv = (int64_t)a.head_dim_k * a.head_dim_v;
+    if (a.state_pool) {
+        const int32_t slot = a.state_idx[n];
+        const bool ok = slot >= 0 && slot < a.num_slots;
+        fin = ok ? a.state_pool + ((int64_t)slot * a.num_heads + h) * kv : nullptr;
+        init = fin;
+    } else {
+        const int64_t off = (n * a.num_heads + h) * kv;
+        init = a.init_state ? a.init_state + off : nullptr;
+        fin = a.final_state ? a.final_state + off : nullptr;
+    }
+}
 
 // One decode step, already validated by the C-ABI layer.
 struct DecodeArgs {

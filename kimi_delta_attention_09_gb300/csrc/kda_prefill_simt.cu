@@ -77,10 +77,12 @@ kda_prefill_simt_kernel(PrefillArgs a)
     int64_t bos, eos;
     clamp_range(a.total_tokens, a.cu_seqlens[n], a.cu_seqlens[n + 1], bos, eos);
 
-    const int64_t state_off = (n * H + h) * (int64_t)(K * V) + vt * kVT;
+    const float *init;
+    float *fin;
+    prefill_state_ptrs(a, n, h, init, fin);
     for (int i = tid; i < K * kVT; i += kSimtThreads) {
         const int c = i / kVT, j = i % kVT;
-        hS[i] = a.init_state ? a.init_state[state_off + (int64_t)c * V + j] : 0.f;
+        hS[i] = init ? init[(int64_t)c * V + vt * kVT + j] : 0.f;
     }
 
     for (int64_t t0 = bos; t0 < eos; t0 += C) {
@@ -191,10 +193,10 @@ kda_prefill_simt_kernel(PrefillArgs a)
         }
     }
     __syncthreads();
-    if (a.final_state) {
+    if (fin) {
         for (int i = tid; i < K * kVT; i += kSimtThreads) {
             const int c = i / kVT, j = i % kVT;
-            a.final_state[state_off + (int64_t)c * V + j] = hS[i];
+            fin[(int64_t)c * V + vt * kVT + j] = hS[i];
         }
     }
 }

@@ -29,7 +29,7 @@
 //   about -0.7 per step sustained over 8 steps) takes an exact-exponential CUDA-core
 //   path for its intra-chunk matrices instead; its result is the same algebra.
 //
-// Mapping: one CTA (8 warps) per (sequence, head, 32-column tile of V); it walks its
+// Mapping: one CTA (16 warps) per (sequence, head, 32-column tile of V); it walks its
 // sequence chunk by chunk.  Per chunk, all warps first build the intra-chunk
 // operands (gate cumsum, factors, A_kk / A_qk with mma.sync, blocked solve), then
 // run the state step on tensor cores; the state tile lives in registers (fp32),
@@ -47,7 +47,7 @@
 namespace kda {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;   // 16 warps
 constexpr int C = kChunk;        // 64 rows per chunk
 constexpr int KD = 128;          // key dim
 constexpr int VD = 128;          // value dim
@@ -63,16 +63,14 @@ constexpr float kFactorMax = 256.f;   // fp16 factor bound (2^8) of the fast pat
 struct Smem {
     static constexpr int q_raw = 0;                          // bf16 [64][128]
     static constexpr int k_raw = q_raw + C * KD * 2;         // bf16 [64][128]
-    static constexpr int g_raw = k_raw + C * KD * 2;         // f32  [64][128] -> G
+    static constexpr int g_raw = k_raw + C * KD * 2;         // f32  [64][128] raw natural-log gate
     static constexpr int v_raw = g_raw + C * KD * 4;         // bf16 [64][32]
     static constexpr int b_raw = v_raw + C * VT * 2;         // f32  [64]
-    static constexpr int a_k = b_raw + C * 4;                // f16 [64][LD128]; later A_kk/T f32 [64][LDA]
-    static constexpr int a_q = a_k + C * LD128 * 2;          // f16 [64][LD128]
-    static constexpr int b_k = a_q + C * LD128 * 2;          // f16 [64][LD128]
-    static constexpr int nkt = b_k + C * LD128 * 2;          // f16 -K~ [64][LD128]
-    static constexpr int qt = nkt + C * LD128 * 2;           // f16  Q~ [64][LD128]
-    static constexpr int kh = qt + C * LD128 * 2;            // f16  K^ [64][LD128] (row i, col c)
-    static constexpr int tm = kh + C * LD128 * 2;            // f16  T  [64][LD64]
+    static constexpr int a_k = b_raw + C * 4;                // f16 k 2^(G - m_R)  [64][LD128]
+    static constexpr int a_q = a_k + C * LD128 * 2;          // f16 q 2^(G - m_R)  [64][LD128]
+    static constexpr int b_k = a_q + C * LD128 * 2;          // f16 k 2^(m_R - G)  [64][LD128]
+    static constexpr int akk = b_k + C * LD128 * 2;          // f32 A_kk [64][LDA]
+    static constexpr int tm = akk + C * LDA * 4;             // f16  T  [64][LD64]
     static constexpr int aqk = tm + C * LD64 * 2;            // f16  A_qk [64][LD64]
     static constexpr int ht = aqk + C * LD64 * 2;            // f16  h^T [32][LD128]
     static constexpr int xt = ht + VT * LD128 * 2;           // f16  (beta X)^T [32][LD64]; xt+dt hold fp16 A_kk in the solve
@@ -80,16 +78,16 @@ struct Smem {
     static constexpr int vs = dt + VT * LD64 * 2;            // f32  V [64][LDV]
     static constexpr int beta = vs + C * LDV * 4;            // f32  [64]
     static constexpr int dec = beta + C * 4;                 // f32  [128] 2^G_last
-    static constexpr int mref = dec + KD * 4;                // f32  [4][128] m_R
-    static constexpr int pm = mref + 4 * KD * 4;             // f32  [4][128] 2^m_R
-    static constexpr int fm = pm + 4 * KD * 4;               // f32  [4][128] 2^(G_last - m_R)
-    static constexpr int rho = fm + 4 * KD * 4;              // f16  [6][128] 2^(m_R - m_I), I < R
-    static constexpr int flag = rho + 6 * KD * 2;            // int
+    static constexpr int pmh = dec + KD * 4;                 // f16  [4][128] 2^m_R
+    static constexpr int fmh = pmh + 4 * KD * 2;             // f16  [4][128] 2^(G_last - m_R)
+    static constexpr int rho = fmh + 4 * KD * 2;             // f16  [6][128] 2^(m_R - m_I), I < R
+    static constexpr int tot8 = rho + 6 * KD * 2;            // f32  [8][128] sums of G over 8-row groups
+    static constexpr int first8 = tot8 + 8 * KD * 4;         // f32  [8][128] first in-group value
+    static constexpr int flag = first8 + 8 * KD * 4;         // int
     static constexpr int mbar = flag + 8;                    // u64 mbarrier of the chunk loads
     static constexpr int total = mbar + 8;
 };
 static_assert(Smem::total <= 232448, "shared memory budget");
-static_assert(C * LDA * 4 <= C * LD128 * 2, "A_kk must fit in the a_k region");
 static_assert(Smem::dt == Smem::xt + VT * LD64 * 2 && 2 * VT == C, "fp16 A_kk spans xt and dt");
 
 // ------------------------------------------------------------------ PTX helpers
@@ -110,6 +108,12 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t 
 {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];\n"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];\n"
+                 : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
 // D += A * B, m16n8k16, fp16 operands, fp32 accumulators
@@ -165,6 +169,26 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
         if (done) return true;
     }
     return false;
+}
+
+// 1/x for x in [2^-8, 2^8] on the FMA pipe: exponent-negating seed, then three
+// Newton-Raphson steps y <- y (2 - x y) (relative error ~1e-7, below fp16 rounding).
+__device__ __forceinline__ float recip_nr(float x)
+{
+    float y = __int_as_float(0x7EF311C3 - __float_as_int(x));
+    y = y * (2.f - x * y);
+    y = y * (2.f - x * y);
+    y = y * (2.f - x * y);
+    return y;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;\n" :: "r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int count)
+{
+    asm volatile("bar.arrive %0, %1;\n" :: "r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -254,20 +278,33 @@ __device__ __forceinline__ void zero_tail_rows(unsigned char *sm, int len, int t
     }
 }
 
-// Exact-exponential intra-chunk matrices for chunks outside the fp16 factor range:
-// A_kk (fp32, into the a_k region) and A_qk (fp16), and the decayed operands
-// -K~, Q~, K^ recomputed with one exponential per element.
+// Exact-exponential intra-chunk matrices for chunks outside the fp16 factor range.
+// Recomputes the exp2-space cumsum G in place in g_raw, then writes A_kk (fp32) and
+// A_qk (fp16) with one exponential per pair and channel, and replaces the operand
+// tiles by the decayed operands themselves (a_k = K~, a_q = Q~, b_k = K^) with unit
+// per-block scales, so the state step reads them unchanged.
 __device__ void exact_intra_chunk(unsigned char *sm, int tid)
 {
     const __nv_bfloat16 *qr = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::q_raw);
     const __nv_bfloat16 *kr = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::k_raw);
-    const float *G = reinterpret_cast<const float *>(sm + Smem::g_raw);
+    float *G = reinterpret_cast<float *>(sm + Smem::g_raw);
     const float *beta = reinterpret_cast<const float *>(sm + Smem::beta);
-    float *akk = reinterpret_cast<float *>(sm + Smem::a_k);
+    float *akk = reinterpret_cast<float *>(sm + Smem::akk);
     __half *aqk = reinterpret_cast<__half *>(sm + Smem::aqk);
-    __half *nkt = reinterpret_cast<__half *>(sm + Smem::nkt);
-    __half *qt = reinterpret_cast<__half *>(sm + Smem::qt);
-    __half *kh = reinterpret_cast<__half *>(sm + Smem::kh);
+    __half *ak = reinterpret_cast<__half *>(sm + Smem::a_k);
+    __half *aq = reinterpret_cast<__half *>(sm + Smem::a_q);
+    __half *bk = reinterpret_cast<__half *>(sm + Smem::b_k);
+    __half *pmh = reinterpret_cast<__half *>(sm + Smem::pmh);
+    __half *fmh = reinterpret_cast<__half *>(sm + Smem::fmh);
+    if (tid < KD) {
+        float acc = 0.f;
+        for (int r = 0; r < C; ++r) { acc += G[r * KD + tid] * kLog2e; G[r * KD + tid] = acc; }
+    }
+    for (int e = tid; e < 4 * KD; e += kThreads) {
+        pmh[e] = __float2half_rn(1.f);
+        fmh[e] = __float2half_rn(1.f);
+    }
+    __syncthreads();
     for (int p = tid; p < C * (C + 1) / 2; p += kThreads) {
         int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
         while (r * (r + 1) / 2 > p) --r;
@@ -289,9 +326,31 @@ __device__ void exact_intra_chunk(unsigned char *sm, int tid)
         const float kv = __bfloat162float(kr[r * KD + c]);
         const float qv = __bfloat162float(qr[r * KD + c]);
         const float eg = exp2f(gr);
-        nkt[r * LD128 + c] = __float2half_rn(-kv * eg);
-        qt[r * LD128 + c] = __float2half_rn(qv * eg);
-        kh[r * LD128 + c] = __float2half_rn(kv * exp2f(gl - gr));
+        ak[r * LD128 + c] = __float2half_rn(kv * eg);
+        aq[r * LD128 + c] = __float2half_rn(qv * eg);
+        bk[r * LD128 + c] = __float2half_rn(kv * exp2f(gl - gr));
+    }
+}
+
+// T_RR = (I + A_RR)^-1 of one 16x16 diagonal block (fp32 forward substitution,
+// lane j owns column j), written to T (fp16) with its zeros and unit diagonal.
+__device__ __forceinline__ void invert_diag_block(const float *akk, __half *tmh, int R, int lane)
+{
+    const int j = lane & 15;
+    float col[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) col[m] = (m == j) ? 1.f : 0.f;
+    const float *Ab = akk + (16 * R) * LDA + 16 * R;
+#pragma unroll
+    for (int r = 1; r < 16; ++r) {
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int m = 0; m < r; ++m) s4[m & 3] += Ab[r * LDA + m] * col[m];
+        if (j < r) col[r] = -((s4[0] + s4[1]) + (s4[2] + s4[3]));
+    }
+    if (lane < 16) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) tmh[(16 * R + r) * LD64 + 16 * R + j] = __float2half_rn(col[r]);
     }
 }
 
@@ -307,7 +366,7 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     const int h = blockIdx.y;
     const int H = a.num_heads;
 
-    float *G = reinterpret_cast<float *>(sm + Smem::g_raw);
+    const float *graw = reinterpret_cast<const float *>(sm + Smem::g_raw);
     const __nv_bfloat16 *qraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::q_raw);
     const __nv_bfloat16 *kraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::k_raw);
     const __nv_bfloat16 *vraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::v_raw);
@@ -315,9 +374,7 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     __half *ak = reinterpret_cast<__half *>(sm + Smem::a_k);
     __half *aq = reinterpret_cast<__half *>(sm + Smem::a_q);
     __half *bk = reinterpret_cast<__half *>(sm + Smem::b_k);
-    __half *nkt = reinterpret_cast<__half *>(sm + Smem::nkt);
-    __half *qt = reinterpret_cast<__half *>(sm + Smem::qt);
-    __half *kh = reinterpret_cast<__half *>(sm + Smem::kh);
+    float *akk = reinterpret_cast<float *>(sm + Smem::akk);
     __half *tmh = reinterpret_cast<__half *>(sm + Smem::tm);
     __half *aqk = reinterpret_cast<__half *>(sm + Smem::aqk);
     __half *ht = reinterpret_cast<__half *>(sm + Smem::ht);
@@ -326,35 +383,38 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     float *vs = reinterpret_cast<float *>(sm + Smem::vs);
     float *beta_s = reinterpret_cast<float *>(sm + Smem::beta);
     float *dec = reinterpret_cast<float *>(sm + Smem::dec);
-    float *mref = reinterpret_cast<float *>(sm + Smem::mref);
-    float *pm = reinterpret_cast<float *>(sm + Smem::pm);
-    float *fm = reinterpret_cast<float *>(sm + Smem::fm);
+    __half *pmh = reinterpret_cast<__half *>(sm + Smem::pmh);
+    __half *fmh = reinterpret_cast<__half *>(sm + Smem::fmh);
     __half *rho = reinterpret_cast<__half *>(sm + Smem::rho);
+    float *tot8 = reinterpret_cast<float *>(sm + Smem::tot8);
+    float *first8 = reinterpret_cast<float *>(sm + Smem::first8);
     volatile int *flag = reinterpret_cast<volatile int *>(sm + Smem::flag);
-    float *akk = reinterpret_cast<float *>(sm + Smem::a_k);       // aliases a_k after P3
 
     int64_t bos, eos;
     clamp_range(a.total_tokens, a.cu_seqlens[n], a.cu_seqlens[n + 1], bos, eos);
 
-    // state-step roles: warp -> (16 value rows mt, quarter qw of chunk rows / key channels)
+    // state-step roles: warp -> (16 value rows mt, eighth qw of chunk rows / key channels):
+    // chunk rows r in [8qw, 8qw+8), key channels c in [16qw, 16qw+16)
     const int mt = warp & 1, qw = warp >> 1;
 
-    // the state tile h^T [v][c] for v in 16mt.., c in 32qw.. : 4 n8-tiles of fp32 accumulators
-    float hreg[4][4];
-    const int64_t state_base = (n * H + h) * (int64_t)(KD * VD) + vt * VT;
+    // the state tile h^T [v][c] for v in 16mt.., c in 16qw.. : 2 n8-tiles of fp32 accumulators
+    float hreg[2][4];
+    const float *init;
+    float *fin;
+    prefill_state_ptrs(a, n, h, init, fin);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int v = 16 * mt + g8 + ((e >> 1) << 3);
-            const int c = 32 * qw + 8 * nt + 2 * tig + (e & 1);
-            hreg[nt][e] = a.init_state ? a.init_state[state_base + (int64_t)c * VD + v] : 0.f;
+            const int c = 16 * qw + 8 * nt + 2 * tig + (e & 1);
+            hreg[nt][e] = init ? init[(int64_t)c * VD + vt * VT + v] : 0.f;
         }
     }
     // fp16 mirror of h^T for the MMAs of the first chunk
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-        const int c = 32 * qw + 8 * nt + 2 * tig;
+    for (int nt = 0; nt < 2; ++nt) {
+        const int c = 16 * qw + 8 * nt + 2 * tig;
         const int v0 = 16 * mt + g8;
         *reinterpret_cast<uint32_t *>(ht + v0 * LD128 + c) = pack_h2(hreg[nt][0], hreg[nt][1]);
         *reinterpret_cast<uint32_t *>(ht + (v0 + 8) * LD128 + c) = pack_h2(hreg[nt][2], hreg[nt][3]);
@@ -382,93 +442,73 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
         if (__syncthreads_or(failed)) { failed = true; break; }
         if (tid == 0) *flag = 0;
 
-        // ---------------- P1: in-chunk gate cumsum, exp2 space (two halves of 32 rows)
-        {
-            const int c = tid & 127, half = tid >> 7;
-            float acc = 0.f;
+        // ---------------- P1: in-chunk gate cumsum, exp2 space; thread = (channel pair, 8-row group E)
+        const int pcp = tid & 63, pE = tid >> 6, pc0 = 2 * pcp;
+        float2 gx[8];
 #pragma unroll
-            for (int r0 = 32 * half; r0 < 32 * half + 32; r0 += 8) {
-                float x[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = G[(r0 + u) * KD + c];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) { acc += x[u] * kLog2e; G[(r0 + u) * KD + c] = acc; }
-            }
+        for (int u = 0; u < 8; ++u) {
+            const float2 g2 = *reinterpret_cast<const float2 *>(graw + (8 * pE + u) * KD + pc0);
+            gx[u] = make_float2(g2.x * kLog2e, g2.y * kLog2e);
         }
-        __syncthreads();
-        if (tid >= 128) {
-            const int c = tid & 127;
-            const float base = G[31 * KD + c];
-#pragma unroll 8
-            for (int r = 32; r < 64; ++r) G[r * KD + c] += base;
-        }
-        __syncthreads();
-        // per-channel scalars
-        if (tid < 128) {
-            const int c = tid;
-            const float gl = G[(C - 1) * KD + c];
-            dec[c] = exp2f(gl);
-            float m[4];
 #pragma unroll
-            for (int R = 0; R < 4; ++R) {
-                m[R] = G[(16 * R + 8) * KD + c];
-                mref[R * KD + c] = m[R];
-                pm[R * KD + c] = exp2f(m[R]);
-                fm[R * KD + c] = exp2f(gl - m[R]);
-            }
-            int p = 0;
-#pragma unroll
-            for (int R = 1; R < 4; ++R)
-#pragma unroll
-                for (int I = 0; I < R; ++I, ++p) rho[p * KD + c] = __float2half_rn(exp2f(m[R] - m[I]));
-        } else if (tid < 128 + C) {
-            beta_s[tid - 128] = braw[tid - 128];
-        }
+        for (int u = 1; u < 8; ++u) { gx[u].x += gx[u - 1].x; gx[u].y += gx[u - 1].y; }
+        *reinterpret_cast<float2 *>(tot8 + pE * KD + pc0) = gx[7];
+        *reinterpret_cast<float2 *>(first8 + pE * KD + pc0) = gx[0];
         for (int e = tid; e < C * VT; e += kThreads) {
             const int r = e >> 5, j = e & 31;
             vs[r * LDV + j] = __bfloat162float(vraw[r * VT + j]);
         }
+        if (tid < C) beta_s[tid] = braw[tid];
         __syncthreads();
 
-        // ---------------- P2: factors and fp16 operands, four channels per thread
+        // ---------------- P2: per-block references, scalars, factors and fp16 operands
         {
-            bool bad = false;
-#pragma unroll 2
-            for (int e = tid; e < C * KD / 4; e += kThreads) {
-                const int r = e >> 5, c = (e & 31) * 4, R = r >> 4;
-                const float4 gv = *reinterpret_cast<const float4 *>(G + r * KD + c);
-                const float4 mv = *reinterpret_cast<const float4 *>(mref + R * KD + c);
-                const float4 pv = *reinterpret_cast<const float4 *>(pm + R * KD + c);
-                const float4 fv = *reinterpret_cast<const float4 *>(fm + R * KD + c);
-                const uint2 kb = *reinterpret_cast<const uint2 *>(kraw + r * KD + c);
-                const uint2 qb = *reinterpret_cast<const uint2 *>(qraw + r * KD + c);
-                const float g4[4] = {gv.x, gv.y, gv.z, gv.w}, m4[4] = {mv.x, mv.y, mv.z, mv.w};
-                const float p4[4] = {pv.x, pv.y, pv.z, pv.w}, f4[4] = {fv.x, fv.y, fv.z, fv.w};
-                const float2 k01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kb.x));
-                const float2 k23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kb.y));
-                const float2 q01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qb.x));
-                const float2 q23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qb.y));
-                const float k4[4] = {k01.x, k01.y, k23.x, k23.y}, q4[4] = {q01.x, q01.y, q23.x, q23.y};
-                float ok[4], oq[4], ob[4], ot[4], oqt[4], okh[4];
+            // prefix sums over the 8-row groups; block references m_R = G(row 16R+8)
+            float2 pre = make_float2(0.f, 0.f), run = make_float2(0.f, 0.f), mAll[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float x = g4[u] - m4[u];
-                    const float em = exp2f(x), ep = exp2f(-x);
-                    bad |= !(em <= kFactorMax && ep <= kFactorMax);
-                    ok[u] = k4[u] * em;
-                    oq[u] = q4[u] * em;
-                    ob[u] = k4[u] * ep;
-                    ot[u] = -ok[u] * p4[u];
-                    oqt[u] = oq[u] * p4[u];
-                    okh[u] = ob[u] * f4[u];
+            for (int E = 0; E < 8; ++E) {
+                const float2 t = *reinterpret_cast<const float2 *>(tot8 + E * KD + pc0);
+                if (E & 1) {
+                    const float2 f = *reinterpret_cast<const float2 *>(first8 + E * KD + pc0);
+                    mAll[E >> 1] = make_float2(run.x + f.x, run.y + f.y);
                 }
-                const int o = r * LD128 + c;
-                *reinterpret_cast<uint2 *>(ak + o) = make_uint2(pack_h2(ok[0], ok[1]), pack_h2(ok[2], ok[3]));
-                *reinterpret_cast<uint2 *>(aq + o) = make_uint2(pack_h2(oq[0], oq[1]), pack_h2(oq[2], oq[3]));
-                *reinterpret_cast<uint2 *>(bk + o) = make_uint2(pack_h2(ob[0], ob[1]), pack_h2(ob[2], ob[3]));
-                *reinterpret_cast<uint2 *>(nkt + o) = make_uint2(pack_h2(ot[0], ot[1]), pack_h2(ot[2], ot[3]));
-                *reinterpret_cast<uint2 *>(qt + o) = make_uint2(pack_h2(oqt[0], oqt[1]), pack_h2(oqt[2], oqt[3]));
-                *reinterpret_cast<uint2 *>(kh + o) = make_uint2(pack_h2(okh[0], okh[1]), pack_h2(okh[2], okh[3]));
+                if (E == pE) pre = run;
+                run.x += t.x; run.y += t.y;
+            }
+            const float2 glast = run;
+            float2 mR = mAll[0];
+#pragma unroll
+            for (int R = 1; R < 4; ++R) if (R == (pE >> 1)) mR = mAll[R];
+            if (pE < 4) {   // per-block scalars of block R = pE, two channels
+                const int R = pE;
+                float2 m = mAll[0];
+#pragma unroll
+                for (int RR = 1; RR < 4; ++RR) if (RR == R) m = mAll[RR];
+                *reinterpret_cast<uint32_t *>(pmh + R * KD + pc0) = pack_h2(exp2f(m.x), exp2f(m.y));
+                *reinterpret_cast<uint32_t *>(fmh + R * KD + pc0) =
+                    pack_h2(exp2f(glast.x - m.x), exp2f(glast.y - m.y));
+#pragma unroll
+                for (int I = 0; I < 3; ++I)
+                    if (I < R)
+                        *reinterpret_cast<uint32_t *>(rho + (R * (R - 1) / 2 + I) * KD + pc0) =
+                            pack_h2(exp2f(m.x - mAll[I].x), exp2f(m.y - mAll[I].y));
+                if (R == 0)
+                    *reinterpret_cast<float2 *>(dec + pc0) = make_float2(exp2f(glast.x), exp2f(glast.y));
+            }
+            const float bx = pre.x - mR.x, by = pre.y - mR.y;   // G_r - m_R = gx + b
+            bool bad = false;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int r = 8 * pE + u;
+                const float emx = exp2f(gx[u].x + bx), emy = exp2f(gx[u].y + by);
+                bad |= !(emx <= kFactorMax && emx >= 1.f / kFactorMax &&
+                         emy <= kFactorMax && emy >= 1.f / kFactorMax);
+                const float epx = recip_nr(emx), epy = recip_nr(emy);
+                const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(kraw + r * KD + pc0));
+                const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qraw + r * KD + pc0));
+                *reinterpret_cast<uint32_t *>(ak + r * LD128 + pc0) = pack_h2(kv.x * emx, kv.y * emy);
+                *reinterpret_cast<uint32_t *>(aq + r * LD128 + pc0) = pack_h2(qv.x * emx, qv.y * emy);
+                *reinterpret_cast<uint32_t *>(bk + r * LD128 + pc0) = pack_h2(kv.x * epx, kv.y * epy);
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) *flag = 1;
         }
@@ -476,79 +516,61 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
         const bool exact_path = *flag != 0;
 
         // ---------------- P3: A_kk and A_qk (lower block triangle) on tensor cores
+        // Ten tasks, one 16x16 block (R, I <= R) each, both matrices per task (the B
+        // fragments of block I serve A_kk and A_qk); warp w % 4 picks the scheduler, so
+        // the tasks are placed three, three, two and two per scheduler.  Warps 10..13
+        // invert the diagonal blocks as soon as the task that owns them has stored them.
         if (!exact_path) {
-            // warp -> (matrix, row block R, up to three 16-column blocks I <= R); the A
-            // fragments of a row block are loaded once per k-step and reused.
-            const int mat = warp >> 2, sub = warp & 3;
-            const __half *A = mat == 0 ? ak : aq;
-            // (R, I) of this warp's column blocks; sub 3 also takes row block 0
-            const int nblk = sub == 2 ? 3 : 2 + (sub == 3);
-            int Rb[3], Ib[3];
-            if (sub == 0)      { Rb[0] = 3; Ib[0] = 0; Rb[1] = 3; Ib[1] = 1; Rb[2] = 3; Ib[2] = 1; }
-            else if (sub == 1) { Rb[0] = 3; Ib[0] = 2; Rb[1] = 3; Ib[1] = 3; Rb[2] = 3; Ib[2] = 3; }
-            else if (sub == 2) { Rb[0] = 2; Ib[0] = 0; Rb[1] = 2; Ib[1] = 1; Rb[2] = 2; Ib[2] = 2; }
-            else               { Rb[0] = 1; Ib[0] = 0; Rb[1] = 1; Ib[1] = 1; Rb[2] = 0; Ib[2] = 0; }
-            float acc[3][2][4];
+            if (warp < 10) {
+                const int R = warp < 4 ? 3 : warp < 7 ? 2 : warp < 9 ? 1 : 0;
+                const int I = warp < 4 ? warp : warp < 7 ? warp - 4 : warp < 9 ? warp - 7 : 0;
+                float acc[2][2][4];   // [matrix][n8 tile][frag]
 #pragma unroll
-            for (int b = 0; b < 3; ++b)
+                for (int m = 0; m < 2; ++m)
 #pragma unroll
-                for (int t = 0; t < 2; ++t) acc[b][t][0] = acc[b][t][1] = acc[b][t][2] = acc[b][t][3] = 0.f;
+                    for (int t = 0; t < 2; ++t) acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
+                const __half *rp = rho + (I < R ? R * (R - 1) / 2 + I : 0) * KD + 2 * tig;
 #pragma unroll
-            for (int ks = 0; ks < KD / 16; ++ks) {
-                uint32_t afr[2][4];
-                ldsm_x4(smem_u32(A + a_off(lane, 16 * Rb[0], 16 * ks, LD128)),
-                        afr[0][0], afr[0][1], afr[0][2], afr[0][3]);
-                if (sub == 3)
-                    ldsm_x4(smem_u32(A + a_off(lane, 0, 16 * ks, LD128)),
-                            afr[1][0], afr[1][1], afr[1][2], afr[1][3]);
+                for (int ks = 0; ks < KD / 16; ++ks) {
+                    uint32_t fk[4], fq[4], bf[4];
+                    ldsm_x4(smem_u32(ak + a_off(lane, 16 * R, 16 * ks, LD128)), fk[0], fk[1], fk[2], fk[3]);
+                    ldsm_x4(smem_u32(aq + a_off(lane, 16 * R, 16 * ks, LD128)), fq[0], fq[1], fq[2], fq[3]);
+                    ldsm_x4(smem_u32(bk + bnk_off(lane, 16 * I, 16 * ks, LD128)), bf[0], bf[1], bf[2], bf[3]);
+                    if (I < R) {
+                        const uint32_t s0 = *reinterpret_cast<const uint32_t *>(rp + 16 * ks);
+                        const uint32_t s1 = *reinterpret_cast<const uint32_t *>(rp + 16 * ks + 8);
+                        bf[0] = hmul2_u32(bf[0], s0); bf[1] = hmul2_u32(bf[1], s1);
+                        bf[2] = hmul2_u32(bf[2], s0); bf[3] = hmul2_u32(bf[3], s1);
+                    }
+                    mma16816(acc[0][0], fk, bf[0], bf[1]);
+                    mma16816(acc[0][1], fk, bf[2], bf[3]);
+                    mma16816(acc[1][0], fq, bf[0], bf[1]);
+                    mma16816(acc[1][1], fq, bf[2], bf[3]);
+                }
 #pragma unroll
-                for (int b = 0; b < 3; ++b) {
-                    if (b < nblk) {
-                        const int R = Rb[b], I = Ib[b];
-                        uint32_t bf[4];
-                        ldsm_x4(smem_u32(bk + bnk_off(lane, 16 * I, 16 * ks, LD128)),
-                                bf[0], bf[1], bf[2], bf[3]);
-                        if (I < R) {
-                            const int pair = R * (R - 1) / 2 + I;
-                            const __half *rp = rho + pair * KD + 16 * ks + 2 * tig;
-                            const uint32_t s0 = *reinterpret_cast<const uint32_t *>(rp);
-                            const uint32_t s1 = *reinterpret_cast<const uint32_t *>(rp + 8);
-                            bf[0] = hmul2_u32(bf[0], s0); bf[1] = hmul2_u32(bf[1], s1);
-                            bf[2] = hmul2_u32(bf[2], s0); bf[3] = hmul2_u32(bf[3], s1);
-                        }
-                        const bool alt = (sub == 3 && b == 2);   // row block 0 of warp sub 3
-                        const uint32_t af[4] = {alt ? afr[1][0] : afr[0][0], alt ? afr[1][1] : afr[0][1],
-                                                alt ? afr[1][2] : afr[0][2], alt ? afr[1][3] : afr[0][3]};
-                        mma16816(acc[b][0], af, bf[0], bf[1]);
-                        mma16816(acc[b][1], af, bf[2], bf[3]);
+                for (int t = 0; t < 2; ++t) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int r = 16 * R + g8 + 8 * hh;
+                        const int i = 16 * I + 8 * t + 2 * tig;
+                        const float k0 = acc[0][t][2 * hh], k1 = acc[0][t][2 * hh + 1];
+                        akk[r * LDA + i] = (i < r) ? beta_s[r] * k0 : 0.f;
+                        akk[r * LDA + i + 1] = (i + 1 < r) ? beta_s[r] * k1 : 0.f;
+                        const float q0 = acc[1][t][2 * hh], q1 = acc[1][t][2 * hh + 1];
+                        *reinterpret_cast<uint32_t *>(aqk + r * LD64 + i) =
+                            pack_h2(i <= r ? q0 : 0.f, i + 1 <= r ? q1 : 0.f);
                     }
                 }
-            }
-            __syncthreads();   // every read of a_k / a_q / b_k is done; a_k becomes A_kk (fp32)
-#pragma unroll
-            for (int b = 0; b < 3; ++b) {
-                if (b < nblk) {
-                    const int R = Rb[b], I = Ib[b];
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) {
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int r = 16 * R + g8 + 8 * hh;
-                            const int i = 16 * I + 8 * t + 2 * tig;
-                            const float v0 = acc[b][t][2 * hh], v1 = acc[b][t][2 * hh + 1];
-                            if (mat == 0) {
-                                akk[r * LDA + i] = (i < r) ? beta_s[r] * v0 : 0.f;
-                                akk[r * LDA + i + 1] = (i + 1 < r) ? beta_s[r] * v1 : 0.f;
-                            } else {
-                                *reinterpret_cast<uint32_t *>(aqk + r * LD64 + i) =
-                                    pack_h2(i <= r ? v0 : 0.f, i + 1 <= r ? v1 : 0.f);
-                            }
-                        }
-                    }
-                }
+                if (I == R) named_bar_arrive(1 + R, 64);   // diagonal block stored
+            } else if (warp < 14) {
+                const int R = warp - 10;
+                named_bar_sync(1 + R, 64);
+                invert_diag_block(akk, tmh, R, lane);
             }
         } else {
             exact_intra_chunk(sm, tid);
+            __syncthreads();
+            if (warp >= 10 && warp < 14) invert_diag_block(akk, tmh, warp - 10, lane);
         }
         __syncthreads();
 
@@ -559,8 +581,8 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
         }
 
         // ---------------- P4: T = (I + A_kk)^-1 in 16x16 blocks
-        // Diagonal blocks: fp32 forward substitution, one warp per block (lane j owns
-        // column j).  Below-diagonal blocks, by distance from the diagonal:
+        // Diagonal blocks were inverted during P3.  Below-diagonal blocks, by distance
+        // from the diagonal:
         //     T_RI = -T_RR sum_{J=I}^{R-1} A_RJ T_JI
         // on tensor cores, evaluated transposed (X^T = sum T_JI^T A_RJ^T, then
         // T_RI^T = -X^T T_RR^T) so X^T passes from accumulator to operand in registers.
@@ -573,24 +595,6 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
                 const int r = 16 * R + rr, m = 16 * J + pp;
                 *reinterpret_cast<uint32_t *>(akh + r * LD64 + m) =
                     pack_h2(akk[r * LDA + m], akk[r * LDA + m + 1]);
-            }
-            if (warp < 4) {
-                const int R = warp, j = lane & 15;
-                float col[16];
-#pragma unroll
-                for (int m = 0; m < 16; ++m) col[m] = (m == j) ? 1.f : 0.f;
-                const float *Ab = akk + (16 * R) * LDA + 16 * R;
-#pragma unroll
-                for (int r = 1; r < 16; ++r) {
-                    float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int m = 0; m < r; ++m) s4[m & 3] += Ab[r * LDA + m] * col[m];
-                    if (j < r) col[r] = -((s4[0] + s4[1]) + (s4[2] + s4[3]));
-                }
-                if (lane < 16) {
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) tmh[(16 * R + r) * LD64 + 16 * R + j] = __float2half_rn(col[r]);
-                }
             }
             __syncthreads();
             for (int lvl = 1; lvl < 4; ++lvl) {
@@ -629,98 +633,98 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
         }
 
         // ---------------- S1: X^T = V^T - h^T K~^T,  O1^T = h^T Q~^T   (rows v of mt, cols r of qw)
-        float xacc[2][4], oacc[2][4];
+        float xacc[4], oacc[4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int e = 0; e < 4; ++e) {
+            const int v = 16 * mt + g8 + ((e >> 1) << 3);
+            const int r = 8 * qw + 2 * tig + (e & 1);
+            xacc[e] = vs[r * LDV + v];
+            oacc[e] = 0.f;
+        }
+        {
+            // B fragments: K~ = a_k 2^m_R and Q~ = a_q 2^m_R, scaled in registers (fp16)
+            const int brow = (8 * qw + (lane & 7)) * LD128 + (((lane >> 3) & 1) << 3);
+            const __half *pmr = pmh + (qw >> 1) * KD + 2 * tig;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int v = 16 * mt + g8 + ((e >> 1) << 3);
-                const int r = 16 * qw + 8 * nt + 2 * tig + (e & 1);
-                xacc[nt][e] = vs[r * LDV + v];
-                oacc[nt][e] = 0.f;
+            for (int ks = 0; ks < KD / 16; ++ks) {
+                uint32_t af[4], bx[2], bq[2];
+                ldsm_x4(smem_u32(ht + a_off(lane, 16 * mt, 16 * ks, LD128)), af[0], af[1], af[2], af[3]);
+                ldsm_x2(smem_u32(ak + brow + 16 * ks), bx[0], bx[1]);
+                ldsm_x2(smem_u32(aq + brow + 16 * ks), bq[0], bq[1]);
+                const uint32_t s0 = *reinterpret_cast<const uint32_t *>(pmr + 16 * ks);
+                const uint32_t s1 = *reinterpret_cast<const uint32_t *>(pmr + 16 * ks + 8);
+                const uint32_t n0 = s0 ^ 0x80008000u, n1 = s1 ^ 0x80008000u;   // -2^m_R
+                mma16816(xacc, af, hmul2_u32(bx[0], n0), hmul2_u32(bx[1], n1));
+                mma16816(oacc, af, hmul2_u32(bq[0], s0), hmul2_u32(bq[1], s1));
             }
         }
-#pragma unroll
-        for (int ks = 0; ks < KD / 16; ++ks) {
-            uint32_t af[4], bx[4], bq[4];
-            ldsm_x4(smem_u32(ht + a_off(lane, 16 * mt, 16 * ks, LD128)), af[0], af[1], af[2], af[3]);
-            ldsm_x4(smem_u32(nkt + bnk_off(lane, 16 * qw, 16 * ks, LD128)), bx[0], bx[1], bx[2], bx[3]);
-            ldsm_x4(smem_u32(qt + bnk_off(lane, 16 * qw, 16 * ks, LD128)), bq[0], bq[1], bq[2], bq[3]);
-            mma16816(xacc[0], af, bx[0], bx[1]);
-            mma16816(xacc[1], af, bx[2], bx[3]);
-            mma16816(oacc[0], af, bq[0], bq[1]);
-            mma16816(oacc[1], af, bq[2], bq[3]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int r = 16 * qw + 8 * nt + 2 * tig;
+        {
+            const int r = 8 * qw + 2 * tig;
             const int v0 = 16 * mt + g8;
             const float b0 = beta_s[r], b1 = beta_s[r + 1];
-            *reinterpret_cast<uint32_t *>(xt + v0 * LD64 + r) = pack_h2(b0 * xacc[nt][0], b1 * xacc[nt][1]);
-            *reinterpret_cast<uint32_t *>(xt + (v0 + 8) * LD64 + r) =
-                pack_h2(b0 * xacc[nt][2], b1 * xacc[nt][3]);
+            *reinterpret_cast<uint32_t *>(xt + v0 * LD64 + r) = pack_h2(b0 * xacc[0], b1 * xacc[1]);
+            *reinterpret_cast<uint32_t *>(xt + (v0 + 8) * LD64 + r) = pack_h2(b0 * xacc[2], b1 * xacc[3]);
         }
         __syncthreads();
 
-        // ---------------- S2: D^T = (beta X)^T T^T  (T lower triangular: k-steps <= qw)
-        float dacc[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) dacc[nt][0] = dacc[nt][1] = dacc[nt][2] = dacc[nt][3] = 0.f;
-        for (int ks = 0; ks <= qw; ++ks) {
-            uint32_t af[4], bt[4];
-            ldsm_x4(smem_u32(xt + a_off(lane, 16 * mt, 16 * ks, LD64)), af[0], af[1], af[2], af[3]);
-            ldsm_x4(smem_u32(tmh + bnk_off(lane, 16 * qw, 16 * ks, LD64)), bt[0], bt[1], bt[2], bt[3]);
-            mma16816(dacc[0], af, bt[0], bt[1]);
-            mma16816(dacc[1], af, bt[2], bt[3]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int r = 16 * qw + 8 * nt + 2 * tig;
+        // ---------------- S2: D^T = (beta X)^T T^T  (T lower triangular: k-blocks <= qw/2)
+        const int rblk = qw >> 1;
+        {
+            float dacc[4] = {0.f, 0.f, 0.f, 0.f};
+            const int brow = (8 * qw + (lane & 7)) * LD64 + (((lane >> 3) & 1) << 3);
+            for (int ks = 0; ks <= rblk; ++ks) {
+                uint32_t af[4], bt[2];
+                ldsm_x4(smem_u32(xt + a_off(lane, 16 * mt, 16 * ks, LD64)), af[0], af[1], af[2], af[3]);
+                ldsm_x2(smem_u32(tmh + brow + 16 * ks), bt[0], bt[1]);
+                mma16816(dacc, af, bt[0], bt[1]);
+            }
+            const int r = 8 * qw + 2 * tig;
             const int v0 = 16 * mt + g8;
-            *reinterpret_cast<uint32_t *>(dt + v0 * LD64 + r) = pack_h2(dacc[nt][0], dacc[nt][1]);
-            *reinterpret_cast<uint32_t *>(dt + (v0 + 8) * LD64 + r) = pack_h2(dacc[nt][2], dacc[nt][3]);
+            *reinterpret_cast<uint32_t *>(dt + v0 * LD64 + r) = pack_h2(dacc[0], dacc[1]);
+            *reinterpret_cast<uint32_t *>(dt + (v0 + 8) * LD64 + r) = pack_h2(dacc[2], dacc[3]);
         }
         __syncthreads();
 
         // ---------------- S3: O^T += D^T A_qk^T ; h^T <- h^T Diag(2^G_last) + D^T K^
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int c = 32 * qw + 8 * nt + 2 * tig;
+        for (int nt = 0; nt < 2; ++nt) {
+            const int c = 16 * qw + 8 * nt + 2 * tig;
             const float d0 = dec[c], d1 = dec[c + 1];
             hreg[nt][0] *= d0; hreg[nt][1] *= d1; hreg[nt][2] *= d0; hreg[nt][3] *= d1;
         }
+        {
+            const int brow = (8 * qw + (lane & 7)) * LD64 + (((lane >> 3) & 1) << 3);
 #pragma unroll
-        for (int ks = 0; ks < C / 16; ++ks) {
-            uint32_t af[4], bk0[4], bk1[4];
-            ldsm_x4(smem_u32(dt + a_off(lane, 16 * mt, 16 * ks, LD64)), af[0], af[1], af[2], af[3]);
-            if (ks <= qw) {
-                uint32_t ba[4];
-                ldsm_x4(smem_u32(aqk + bnk_off(lane, 16 * qw, 16 * ks, LD64)), ba[0], ba[1], ba[2], ba[3]);
-                mma16816(oacc[0], af, ba[0], ba[1]);
-                mma16816(oacc[1], af, ba[2], ba[3]);
+            for (int ks = 0; ks < C / 16; ++ks) {
+                uint32_t af[4], bk0[4];
+                ldsm_x4(smem_u32(dt + a_off(lane, 16 * mt, 16 * ks, LD64)), af[0], af[1], af[2], af[3]);
+                if (ks <= rblk) {
+                    uint32_t ba[2];
+                    ldsm_x2(smem_u32(aqk + brow + 16 * ks), ba[0], ba[1]);
+                    mma16816(oacc, af, ba[0], ba[1]);
+                }
+                // K^ = b_k 2^(G_last - m_R), R = ks: one scale per key channel (n index)
+                ldsm_x4_t(smem_u32(bk + bkn_off(lane, 16 * ks, 16 * qw, LD128)), bk0[0], bk0[1], bk0[2], bk0[3]);
+                const __half f0 = fmh[ks * KD + 16 * qw + g8], f1 = fmh[ks * KD + 16 * qw + 8 + g8];
+                const __half2 f00 = __halves2half2(f0, f0), f11 = __halves2half2(f1, f1);
+                const uint32_t u0 = *reinterpret_cast<const uint32_t *>(&f00);
+                const uint32_t u1 = *reinterpret_cast<const uint32_t *>(&f11);
+                mma16816(hreg[0], af, hmul2_u32(bk0[0], u0), hmul2_u32(bk0[1], u0));
+                mma16816(hreg[1], af, hmul2_u32(bk0[2], u1), hmul2_u32(bk0[3], u1));
             }
-            ldsm_x4_t(smem_u32(kh + bkn_off(lane, 16 * ks, 32 * qw, LD128)), bk0[0], bk0[1], bk0[2], bk0[3]);
-            ldsm_x4_t(smem_u32(kh + bkn_off(lane, 16 * ks, 32 * qw + 16, LD128)), bk1[0], bk1[1], bk1[2], bk1[3]);
-            mma16816(hreg[0], af, bk0[0], bk0[1]);
-            mma16816(hreg[1], af, bk0[2], bk0[3]);
-            mma16816(hreg[2], af, bk1[0], bk1[1]);
-            mma16816(hreg[3], af, bk1[2], bk1[3]);
         }
         // output rows of this chunk
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int v = 16 * mt + g8 + ((e >> 1) << 3);
-                const int r = 16 * qw + 8 * nt + 2 * tig + (e & 1);
-                if (r < len)
-                    out[((t0 + r) * H + h) * VD + vt * VT + v] = from_f32<Tout>(a.scale * oacc[nt][e]);
-            }
+        for (int e = 0; e < 4; ++e) {
+            const int v = 16 * mt + g8 + ((e >> 1) << 3);
+            const int r = 8 * qw + 2 * tig + (e & 1);
+            if (r < len)
+                out[((t0 + r) * H + h) * VD + vt * VT + v] = from_f32<Tout>(a.scale * oacc[e]);
         }
         // fp16 mirror of the new state for the next chunk
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int c = 32 * qw + 8 * nt + 2 * tig;
+        for (int nt = 0; nt < 2; ++nt) {
+            const int c = 16 * qw + 8 * nt + 2 * tig;
             const int v0 = 16 * mt + g8;
             *reinterpret_cast<uint32_t *>(ht + v0 * LD128 + c) = pack_h2(hreg[nt][0], hreg[nt][1]);
             *reinterpret_cast<uint32_t *>(ht + (v0 + 8) * LD128 + c) = pack_h2(hreg[nt][2], hreg[nt][3]);
@@ -732,18 +736,18 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
         // error marker: NaN state; the copies still in flight get one more bounded wait
         mbar_wait(mbar, load_parity);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) hreg[nt][e] = __int_as_float(0x7fc00000);
     }
-    if (a.final_state) {
+    if (fin) {
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
+        for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int v = 16 * mt + g8 + ((e >> 1) << 3);
-                const int c = 32 * qw + 8 * nt + 2 * tig + (e & 1);
-                a.final_state[state_base + (int64_t)c * VD + v] = hreg[nt][e];
+                const int c = 16 * qw + 8 * nt + 2 * tig + (e & 1);
+                fin[(int64_t)c * VD + vt * VT + v] = hreg[nt][e];
             }
         }
     }

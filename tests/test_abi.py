@@ -124,6 +124,30 @@ def test_prefill_alias_guard(native):
     assert _prefill(native, out=BASE + (8 << 24) + 64) == native.KDA_ERR_ALIAS
 
 
+def _prefill_paged(native, **kw):
+    a = dict(q=BASE, k=BASE + (1 << 24), v=BASE + (2 << 24), g=BASE + (3 << 24),
+             beta=BASE + (4 << 24), scale=0.125, pool=BASE + (1 << 32), idx=BASE + (5 << 24),
+             cu=BASE + (6 << 24), out=BASE + (7 << 24), T=100, N=2, S=8, H=2, K=128, V=128,
+             dtype=1, out_dtype=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return native.lib.kda_chunk_prefill_paged(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
+        vp(a["pool"]), vp(a["idx"]), vp(a["cu"]), vp(a["out"]), a["T"], a["N"], a["S"], a["H"],
+        a["K"], a["V"], a["dtype"], a["out_dtype"], None)
+
+
+def test_paged_prefill_validation_and_alias(native):
+    assert _prefill_paged(native, idx=None) == native.KDA_ERR_INVALID_ARG
+    assert _prefill_paged(native, pool=None) == native.KDA_ERR_INVALID_ARG
+    assert _prefill_paged(native, S=-1) == native.KDA_ERR_INVALID_ARG
+    assert _prefill_paged(native, K=96) == native.KDA_ERR_UNSUPPORTED
+    assert _prefill_paged(native, N=0) == native.KDA_OK
+    assert _prefill_paged(native, out=BASE + (1 << 32) + 512) == native.KDA_ERR_ALIAS
+    assert _prefill_paged(native, pool=BASE + (2 << 24)) == native.KDA_ERR_ALIAS
+    assert _prefill_paged(native, idx=BASE + (1 << 32) + 64) == native.KDA_ERR_ALIAS
+
+
 def test_decode_argument_validation_and_alias(native):
     assert _decode(native, idx=None) == native.KDA_ERR_INVALID_ARG
     assert _decode(native, pool=None) == native.KDA_ERR_INVALID_ARG
