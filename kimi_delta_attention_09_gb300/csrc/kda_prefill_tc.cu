@@ -30,12 +30,14 @@
 //   path for its intra-chunk matrices instead; its result is the same algebra.
 //
 // Mapping: one CTA (16 warps) per (sequence, head, 32-column tile of V); it walks its
-// sequence chunk by chunk.  Per chunk, all warps first build the intra-chunk
-// operands (gate cumsum, factors, A_kk / A_qk with mma.sync, blocked solve), then
-// run the state step on tensor cores; the state tile lives in registers (fp32),
-// mirrored to shared memory in fp16 as the next chunk's MMA operand.  The raw
-// inputs of chunk j+1 are fetched with cp.async while chunk j's solve and state
-// step run.
+// sequence chunk by chunk.  The raw inputs of a chunk arrive as TMA tiles (issued one
+// chunk ahead by a dedicated warp).  Per chunk, the warps build the intra-chunk
+// operands (gate cumsum, factors, A_kk / A_qk with mma.sync, blocked solve), then run
+// the state step: the state tile h^T (fp32, 128 key channels x 32 values) lives in
+// tensor memory, and the two big contractions of the step are tcgen05 MMAs issued by
+// one thread -- [-K~; Q~] h (X and the inter-chunk part of o) and K^^T D accumulated
+// into the state, with A_qk D accumulated into o.  The small D = T (beta X) product
+// stays on mma.sync.  tcgen05 operands use the 128-byte-swizzled K-major layout.
 #include <cstring>
 
 #include <cuda.h>
@@ -55,40 +57,46 @@ constexpr int VT = 32;           // value columns per CTA
 constexpr int kVTiles = VD / VT;
 constexpr int LD128 = KD + 8;    // f16 row stride (halves) of 128-column tiles: 272 B
 constexpr int LD64 = C + 8;      // f16 row stride of 64-column tiles: 144 B
-constexpr int LDV = VT + 1;      // fp32 V tile stride
-constexpr int LDA = C + 1;       // fp32 A_kk / T stride
 constexpr float kFactorMax = 256.f;   // fp16 factor bound (2^8) of the fast path
 
-// Shared memory map (byte offsets).
+// Shared memory map (byte offsets).  SW128 tiles: 128-byte-swizzled K-major tcgen05
+// operands (1024-byte aligned); the others are padded row-major mma.sync operands.
 struct Smem {
     static constexpr int q_raw = 0;                          // bf16 [64][128]
     static constexpr int k_raw = q_raw + C * KD * 2;         // bf16 [64][128]
     static constexpr int g_raw = k_raw + C * KD * 2;         // f32  [64][128] raw natural-log gate
     static constexpr int v_raw = g_raw + C * KD * 4;         // bf16 [64][32]
-    static constexpr int b_raw = v_raw + C * VT * 2;         // f32  [64]
-    static constexpr int a_k = b_raw + C * 4;                // f16 k 2^(G - m_R)  [64][LD128]
+    static constexpr int b_raw = v_raw + C * VT * 2;         // f32  [64][4] beta of heads 4*(h/4)..
+    static constexpr int a_k = b_raw + C * 4 * 4;            // f16 k 2^(G - m_R)  [64][LD128]
     static constexpr int a_q = a_k + C * LD128 * 2;          // f16 q 2^(G - m_R)  [64][LD128]
     static constexpr int b_k = a_q + C * LD128 * 2;          // f16 k 2^(m_R - G)  [64][LD128]
-    static constexpr int akk = b_k + C * LD128 * 2;          // f32 A_kk [64][LDA]
-    static constexpr int tm = akk + C * LDA * 4;             // f16  T  [64][LD64]
-    static constexpr int aqk = tm + C * LD64 * 2;            // f16  A_qk [64][LD64]
-    static constexpr int ht = aqk + C * LD64 * 2;            // f16  h^T [32][LD128]
-    static constexpr int xt = ht + VT * LD128 * 2;           // f16  (beta X)^T [32][LD64]; xt+dt hold fp16 A_kk in the solve
-    static constexpr int dt = xt + VT * LD64 * 2;            // f16  D^T [32][LD64]
-    static constexpr int vs = dt + VT * LD64 * 2;            // f32  V [64][LDV]
-    static constexpr int beta = vs + C * LDV * 4;            // f32  [64]
+    static constexpr int tm = b_k + C * LD128 * 2;           // f16  T  [64][LD64]
+    static constexpr int a1 = (tm + C * LD64 * 2 + 1023) / 1024 * 1024;   // SW128 [-K~; Q~] 128 x 128
+    static constexpr int kht = a1 + 2 * C * KD * 2;          // SW128 K^^T: 128 (channel) x 64 (row)
+    static constexpr int akh = kht + KD * C * 2;             // SW128 A_kk fp16 64 x 64
+    static constexpr int aqk = akh + C * C * 2;              // SW128 A_qk fp16 64 x 64 (follows akh:
+                                                             // [akh; aqk] is the 128-row A of o += A_qk D)
+    static constexpr int ht = aqk + C * C * 2;               // SW128 h^T fp16 32 (value) x 128 (channel)
+    static constexpr int dt = ht + VT * KD * 2;              // SW128 D^T fp16 32 (value) x 64 (row)
+    static constexpr int xt = dt + VT * C * 2;               // f16 (beta X)^T [32][LD64]
+    static constexpr int tot8 = dt;                          // f32 [8][128] group sums (P1/P2 only)
+    static constexpr int first8 = xt;                        // f32 [8][128] group firsts (P1/P2 only)
+    static constexpr int vs = xt + VT * LD64 * 2;            // bf16 V [64][32]
+    static constexpr int beta = vs + C * VT * 2;             // f32  [64]
     static constexpr int dec = beta + C * 4;                 // f32  [128] 2^G_last
-    static constexpr int pmh = dec + KD * 4;                 // f16  [4][128] 2^m_R
-    static constexpr int fmh = pmh + 4 * KD * 2;             // f16  [4][128] 2^(G_last - m_R)
-    static constexpr int rho = fmh + 4 * KD * 2;             // f16  [6][128] 2^(m_R - m_I), I < R
-    static constexpr int tot8 = rho + 6 * KD * 2;            // f32  [8][128] sums of G over 8-row groups
-    static constexpr int first8 = tot8 + 8 * KD * 4;         // f32  [8][128] first in-group value
-    static constexpr int flag = first8 + 8 * KD * 4;         // int
+    static constexpr int rho = dec + KD * 4;                 // f16  [6][128] 2^(m_R - m_I), I < R
+    static constexpr int flag = rho + 6 * KD * 2;            // int
     static constexpr int mbar = flag + 8;                    // u64 mbarrier of the chunk loads
-    static constexpr int total = mbar + 8;
+    static constexpr int mbar_mma = mbar + 8;                // u64 mbarrier of the tcgen05 MMAs
+    static constexpr int tmem = mbar_mma + 8;                // u32 tensor-memory base
+    static constexpr int total = tmem + 8;
 };
 static_assert(Smem::total <= 232448, "shared memory budget");
-static_assert(Smem::dt == Smem::xt + VT * LD64 * 2 && 2 * VT == C, "fp16 A_kk spans xt and dt");
+static_assert(Smem::a1 % 1024 == 0 && Smem::kht % 1024 == 0 && Smem::akh % 1024 == 0 &&
+              Smem::aqk % 1024 == 0 && Smem::ht % 1024 == 0 && Smem::dt % 1024 == 0,
+              "SW128 tiles need 1024-byte alignment");
+static_assert(Smem::first8 + 8 * KD * 4 <= Smem::vs + C * VT * 2 && Smem::tot8 + 8 * KD * 4 <= Smem::xt,
+              "gate group sums fit in the D^T / (beta X)^T space");
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -146,6 +154,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t mbar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];\n"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" :: "r"(mbar), "r"(count) : "memory");
@@ -200,6 +218,84 @@ __device__ __forceinline__ void cp_async_wait_all()
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
 }
 
+// ------------------------------------------------------------------ tcgen05 helpers
+// Element (row, k) of a 128-byte-swizzled K-major tile of `rows` rows, in halves:
+// 64-element column blocks stacked after all rows; within a block, row r is 128 B
+// and its 16-byte chunk j sits at chunk j ^ (r % 8).
+__device__ __forceinline__ int sw128(int row, int k, int rows)
+{
+    return ((k >> 6) * rows + row) * 64 + ((((k >> 3) & 7) ^ (row & 7)) << 3) + (k & 7);
+}
+
+// Shared-memory matrix descriptor of a SW128 K-major operand starting at `saddr`:
+// 8-row groups 1024 B apart, descriptor version 1, layout SWIZZLE_128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// descriptor of k16-step ks of a SW128 tile with `rows` rows at `base`
+__device__ __forceinline__ uint64_t sw128_kdesc(uint32_t base, int ks, int rows)
+{
+    return sw128_desc(base + (uint32_t)((ks >> 2) * rows * 128 + (ks & 3) * 32));
+}
+
+// instruction descriptor: fp16 A and B (K-major), fp32 D, M = 128, N = 32
+constexpr uint32_t kIdescM128N32 = (1u << 4) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                 :: "r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t mbar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+                 :: "r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+
+// 32 lanes x 16 columns of fp32 from / to tensor memory
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+                   "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+                 :: "r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])),
+                    "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])),
+                    "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+                    "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+                    "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+                    "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+                 : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -223,43 +319,45 @@ __device__ __forceinline__ int bnk_off(int lane, int n0, int k0, int ld)
 {
     return (n0 + (lane & 7) + ((lane >> 4) << 3)) * ld + k0 + (((lane >> 3) & 1) << 3);
 }
-// B operand stored [k][n] (n contiguous), read transposed: two n-tiles at (k0, n0).
-__device__ __forceinline__ int bkn_off(int lane, int k0, int n0, int ld)
-{
-    return (k0 + (lane & 7) + (((lane >> 3) & 1) << 3)) * ld + n0 + ((lane >> 4) << 3);
-}
 
 // Tensor maps of q, k, g (box 128 channels x 1 head x 64 tokens) and v (box 32
 // columns x 1 head x 64 tokens), built on the host for each call.
 struct TmaMaps {
-    CUtensorMap q, k, g, v;
+    CUtensorMap q, k, g, v, beta;   // beta: [T, H] fp32, box 4 heads x 64 tokens (H % 4 == 0)
+    int beta_tma;                   // 0: beta comes by 4-byte cp.async instead
 };
 
 // ------------------------------------------------------------------ loads
-// Tokens [t0, t0+64) of q, k, g and of this CTA's 32 v columns arrive as four TMA
-// tiles that complete on the chunk mbarrier (rows past the end of the tensor are
+// Tokens [t0, t0+64) of q, k, g, of this CTA's 32 v columns and of beta arrive as
+// TMA tiles that complete on the chunk mbarrier (rows past the end of the tensor are
 // zero-filled by the TMA unit; rows past the end of the SEQUENCE are zeroed after
-// arrival, see zero_tail_rows).  beta (strided by H) uses 4-byte cp.async.  Called
-// by all threads after a barrier that ends every read of the raw buffers.
+// arrival, see zero_tail_rows).  When H is not a multiple of 4, beta (strided by H)
+// comes by 4-byte cp.async instead.  Called by ONE warp after a barrier that ends
+// every read of the raw buffers.
 __device__ __forceinline__ void issue_chunk_loads(unsigned char *sm, const PrefillArgs &a,
                                                   const TmaMaps &maps, int64_t t0, int len,
-                                                  int h, int vt, int tid)
+                                                  int h, int vt, int lane)
 {
-    if (tid < C) {
-        const int valid = tid < len;
-        const int64_t row = t0 + (valid ? tid : 0);
-        cp_async4(smem_u32(sm + Smem::b_raw + tid * 4), a.beta + row * a.num_heads + h, valid ? 4 : 0);
+    float *braw = reinterpret_cast<float *>(sm + Smem::b_raw);
+    if (!maps.beta_tma) {
+        for (int r = lane; r < C; r += 32) {
+            const int valid = r < len;
+            const int64_t row = t0 + (valid ? r : 0);
+            cp_async4(smem_u32(braw + r * 4), a.beta + row * a.num_heads + h, valid ? 4 : 0);
+        }
     }
     cp_async_commit();
-    if (tid == 0) {
+    if (lane == 0) {
         const uint32_t mbar = smem_u32(sm + Smem::mbar);
         fence_proxy_async_smem();   // earlier generic reads of the raw buffers come first
-        mbar_arrive_expect_tx(mbar, C * (2 * KD * 2 + KD * 4 + VT * 2));
+        const uint32_t bytes = C * (2 * KD * 2 + KD * 4 + VT * 2) + (maps.beta_tma ? C * 16 : 0);
+        mbar_arrive_expect_tx(mbar, bytes);
         const int z = (int)t0;
         tma_load_3d(smem_u32(sm + Smem::q_raw), &maps.q, 0, h, z, mbar);
         tma_load_3d(smem_u32(sm + Smem::k_raw), &maps.k, 0, h, z, mbar);
         tma_load_3d(smem_u32(sm + Smem::g_raw), &maps.g, 0, h, z, mbar);
         tma_load_3d(smem_u32(sm + Smem::v_raw), &maps.v, vt * VT, h, z, mbar);
+        if (maps.beta_tma) tma_load_2d(smem_u32(braw), &maps.beta, h & ~3, z, mbar);
     }
 }
 
@@ -278,31 +376,44 @@ __device__ __forceinline__ void zero_tail_rows(unsigned char *sm, int len, int t
     }
 }
 
+// scale * v[0..16) to 16 contiguous outputs (16-byte stores)
+__device__ __forceinline__ void store_row16(float *dst, const float (&v)[16], float scale)
+{
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        reinterpret_cast<float4 *>(dst)[j] =
+            make_float4(scale * v[4 * j], scale * v[4 * j + 1], scale * v[4 * j + 2], scale * v[4 * j + 3]);
+}
+__device__ __forceinline__ void store_row16(__nv_bfloat16 *dst, const float (&v)[16], float scale)
+{
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        uint4 w;
+        __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            p[u] = __floats2bfloat162_rn(scale * v[8 * j + 2 * u], scale * v[8 * j + 2 * u + 1]);
+        reinterpret_cast<uint4 *>(dst)[j] = w;
+    }
+}
+
 // Exact-exponential intra-chunk matrices for chunks outside the fp16 factor range.
-// Recomputes the exp2-space cumsum G in place in g_raw, then writes A_kk (fp32) and
-// A_qk (fp16) with one exponential per pair and channel, and replaces the operand
-// tiles by the decayed operands themselves (a_k = K~, a_q = Q~, b_k = K^) with unit
-// per-block scales, so the state step reads them unchanged.
+// Recomputes the exp2-space cumsum G in place in g_raw, then writes A_kk and A_qk
+// (fp16) with one exponential per pair and channel, and the state-step operands
+// -K~, Q~ and K^^T with one exponential per element.
 __device__ void exact_intra_chunk(unsigned char *sm, int tid)
 {
     const __nv_bfloat16 *qr = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::q_raw);
     const __nv_bfloat16 *kr = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::k_raw);
     float *G = reinterpret_cast<float *>(sm + Smem::g_raw);
     const float *beta = reinterpret_cast<const float *>(sm + Smem::beta);
-    float *akk = reinterpret_cast<float *>(sm + Smem::akk);
+    __half *akh = reinterpret_cast<__half *>(sm + Smem::akh);
     __half *aqk = reinterpret_cast<__half *>(sm + Smem::aqk);
-    __half *ak = reinterpret_cast<__half *>(sm + Smem::a_k);
-    __half *aq = reinterpret_cast<__half *>(sm + Smem::a_q);
-    __half *bk = reinterpret_cast<__half *>(sm + Smem::b_k);
-    __half *pmh = reinterpret_cast<__half *>(sm + Smem::pmh);
-    __half *fmh = reinterpret_cast<__half *>(sm + Smem::fmh);
+    __half *a1 = reinterpret_cast<__half *>(sm + Smem::a1);
+    __half *kht = reinterpret_cast<__half *>(sm + Smem::kht);
     if (tid < KD) {
         float acc = 0.f;
         for (int r = 0; r < C; ++r) { acc += G[r * KD + tid] * kLog2e; G[r * KD + tid] = acc; }
-    }
-    for (int e = tid; e < 4 * KD; e += kThreads) {
-        pmh[e] = __float2half_rn(1.f);
-        fmh[e] = __float2half_rn(1.f);
     }
     __syncthreads();
     for (int p = tid; p < C * (C + 1) / 2; p += kThreads) {
@@ -316,9 +427,12 @@ __device__ void exact_intra_chunk(unsigned char *sm, int tid)
             sk += __bfloat162float(kr[r * KD + c]) * kic;
             sq += __bfloat162float(qr[r * KD + c]) * kic;
         }
-        akk[r * LDA + i] = (i < r) ? beta[r] * sk : 0.f;
-        aqk[r * LD64 + i] = __float2half_rn(sq);
-        if (i < r) aqk[i * LD64 + r] = __float2half_rn(0.f);
+        akh[sw128(r, i, C)] = __float2half_rn((i < r) ? beta[r] * sk : 0.f);
+        aqk[sw128(r, i, C)] = __float2half_rn(sq);
+        if (i < r) {
+            akh[sw128(i, r, C)] = __float2half_rn(0.f);
+            aqk[sw128(i, r, C)] = __float2half_rn(0.f);
+        }
     }
     for (int e = tid; e < C * KD; e += kThreads) {
         const int r = e >> 7, c = e & 127;
@@ -326,26 +440,26 @@ __device__ void exact_intra_chunk(unsigned char *sm, int tid)
         const float kv = __bfloat162float(kr[r * KD + c]);
         const float qv = __bfloat162float(qr[r * KD + c]);
         const float eg = exp2f(gr);
-        ak[r * LD128 + c] = __float2half_rn(kv * eg);
-        aq[r * LD128 + c] = __float2half_rn(qv * eg);
-        bk[r * LD128 + c] = __float2half_rn(kv * exp2f(gl - gr));
+        a1[sw128(r, c, 2 * C)] = __float2half_rn(-kv * eg);
+        a1[sw128(C + r, c, 2 * C)] = __float2half_rn(qv * eg);
+        kht[sw128(c, r, KD)] = __float2half_rn(kv * exp2f(gl - gr));
     }
 }
 
-// T_RR = (I + A_RR)^-1 of one 16x16 diagonal block (fp32 forward substitution,
-// lane j owns column j), written to T (fp16) with its zeros and unit diagonal.
-__device__ __forceinline__ void invert_diag_block(const float *akk, __half *tmh, int R, int lane)
+// T_RR = (I + A_RR)^-1 of one 16x16 diagonal block (fp32 forward substitution on the
+// fp16 A_kk, lane j owns column j), written to T (fp16) with its zeros and unit diagonal.
+__device__ __forceinline__ void invert_diag_block(const __half *akh, __half *tmh, int R, int lane)
 {
     const int j = lane & 15;
     float col[16];
 #pragma unroll
     for (int m = 0; m < 16; ++m) col[m] = (m == j) ? 1.f : 0.f;
-    const float *Ab = akk + (16 * R) * LDA + 16 * R;
 #pragma unroll
     for (int r = 1; r < 16; ++r) {
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < r; ++m) s4[m & 3] += Ab[r * LDA + m] * col[m];
+        for (int m = 0; m < r; ++m)
+            s4[m & 3] += __half2float(akh[sw128(16 * R + r, 16 * R + m, C)]) * col[m];
         if (j < r) col[r] = -((s4[0] + s4[1]) + (s4[2] + s4[3]));
     }
     if (lane < 16) {
@@ -358,7 +472,7 @@ template <typename Tout>
 __global__ void __launch_bounds__(kThreads, 1)
 kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
 {
-    extern __shared__ __align__(128) unsigned char sm[];
+    extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g8 = lane >> 2, tig = lane & 3;
     const int64_t n = blockIdx.x / kVTiles;
@@ -369,22 +483,21 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     const float *graw = reinterpret_cast<const float *>(sm + Smem::g_raw);
     const __nv_bfloat16 *qraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::q_raw);
     const __nv_bfloat16 *kraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::k_raw);
-    const __nv_bfloat16 *vraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::v_raw);
     const float *braw = reinterpret_cast<const float *>(sm + Smem::b_raw);
     __half *ak = reinterpret_cast<__half *>(sm + Smem::a_k);
     __half *aq = reinterpret_cast<__half *>(sm + Smem::a_q);
     __half *bk = reinterpret_cast<__half *>(sm + Smem::b_k);
-    float *akk = reinterpret_cast<float *>(sm + Smem::akk);
     __half *tmh = reinterpret_cast<__half *>(sm + Smem::tm);
+    __half *a1 = reinterpret_cast<__half *>(sm + Smem::a1);
+    __half *kht = reinterpret_cast<__half *>(sm + Smem::kht);
+    __half *akh = reinterpret_cast<__half *>(sm + Smem::akh);
     __half *aqk = reinterpret_cast<__half *>(sm + Smem::aqk);
     __half *ht = reinterpret_cast<__half *>(sm + Smem::ht);
-    __half *xt = reinterpret_cast<__half *>(sm + Smem::xt);
     __half *dt = reinterpret_cast<__half *>(sm + Smem::dt);
-    float *vs = reinterpret_cast<float *>(sm + Smem::vs);
+    __half *xt = reinterpret_cast<__half *>(sm + Smem::xt);
+    __nv_bfloat16 *vs = reinterpret_cast<__nv_bfloat16 *>(sm + Smem::vs);
     float *beta_s = reinterpret_cast<float *>(sm + Smem::beta);
     float *dec = reinterpret_cast<float *>(sm + Smem::dec);
-    __half *pmh = reinterpret_cast<__half *>(sm + Smem::pmh);
-    __half *fmh = reinterpret_cast<__half *>(sm + Smem::fmh);
     __half *rho = reinterpret_cast<__half *>(sm + Smem::rho);
     float *tot8 = reinterpret_cast<float *>(sm + Smem::tot8);
     float *first8 = reinterpret_cast<float *>(sm + Smem::first8);
@@ -392,54 +505,73 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
 
     int64_t bos, eos;
     clamp_range(a.total_tokens, a.cu_seqlens[n], a.cu_seqlens[n + 1], bos, eos);
-
-    // state-step roles: warp -> (16 value rows mt, eighth qw of chunk rows / key channels):
-    // chunk rows r in [8qw, 8qw+8), key channels c in [16qw, 16qw+16)
-    const int mt = warp & 1, qw = warp >> 1;
-
-    // the state tile h^T [v][c] for v in 16mt.., c in 16qw.. : 2 n8-tiles of fp32 accumulators
-    float hreg[2][4];
     const float *init;
     float *fin;
     prefill_state_ptrs(a, n, h, init, fin);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int v = 16 * mt + g8 + ((e >> 1) << 3);
-            const int c = 16 * qw + 8 * nt + 2 * tig + (e & 1);
-            hreg[nt][e] = init ? init[(int64_t)c * VD + vt * VT + v] : 0.f;
-        }
+
+    // ---- tensor memory (64 columns: [0, 32) the step accumulator D1, [32, 64) the state
+    //      h^T with lane = key channel, column = value) and the two mbarriers
+    const uint32_t mbar = smem_u32(sm + Smem::mbar);
+    const uint32_t mbar_mma = smem_u32(sm + Smem::mbar_mma);
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
+                     :: "r"(smem_u32(sm + Smem::tmem)), "r"(64) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
-    // fp16 mirror of h^T for the MMAs of the first chunk
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        mbar_init(mbar_mma, 1);
+    }
+    // A_qk blocks above the diagonal are never written by the fast path; zero them once
+    for (int e = tid; e < C * C; e += kThreads) {
+        const int r = e >> 6, i = e & 63;
+        if ((i >> 4) > (r >> 4)) aqk[sw128(r, i, C)] = __float2half_rn(0.f);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Smem::tmem);
+    const uint32_t tD1 = tmem, tH = tmem + 32;
+
+    // TMEM epilogue roles (warp w reaches lanes 32 (w % 4) .. +31):
+    //   state warps 8..15: key channels sc = 32 (w % 4) + lane, value columns [16 hc, 16 hc + 16)
+    //   X rows (lanes 0..63): warps 0, 1 (columns 0..15) and 4, 5 (columns 16..31)
+    //   o rows (lanes 64..127): warps 2, 3 (columns 0..15) and 6, 7 (columns 16..31)
+    const bool state_warp = warp >= 8;
+    const int sc = 32 * (warp & 3) + lane;                       // key channel of a state warp
+    const int hc = (warp >> 2) & 1;                              // its half of the value columns
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // TMEM lane quadrant
+    if (state_warp) {   // initial state -> tensor memory and its fp16 mirror
+        float hv[16];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int c = 16 * qw + 8 * nt + 2 * tig;
-        const int v0 = 16 * mt + g8;
-        *reinterpret_cast<uint32_t *>(ht + v0 * LD128 + c) = pack_h2(hreg[nt][0], hreg[nt][1]);
-        *reinterpret_cast<uint32_t *>(ht + (v0 + 8) * LD128 + c) = pack_h2(hreg[nt][2], hreg[nt][3]);
+        for (int j = 0; j < 4; ++j) {
+            const float4 x = init ? *reinterpret_cast<const float4 *>(init + (int64_t)sc * VD + vt * VT + 16 * hc + 4 * j)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            hv[4 * j] = x.x; hv[4 * j + 1] = x.y; hv[4 * j + 2] = x.z; hv[4 * j + 3] = x.w;
+        }
+        tmem_st16(tH + lane_off + 16 * hc, hv);
+#pragma unroll
+        for (int v = 0; v < 16; ++v) ht[sw128(16 * hc + v, sc, VT)] = __float2half_rn(hv[v]);
+        fence_proxy_async_smem();
+        tc_fence_before();
     }
 
-    const uint32_t mbar = smem_u32(sm + Smem::mbar);
-    if (tid == 0) mbar_init(mbar, 1);
-    __syncthreads();
-    if (bos < eos) issue_chunk_loads(sm, a, maps, bos, (int)((eos - bos) < C ? (eos - bos) : C), h, vt, tid);
+    constexpr int kLoadWarp = kThreads / 32 - 1;   // issues every chunk's loads
+    if (bos < eos && warp == kLoadWarp)
+        issue_chunk_loads(sm, a, maps, bos, (int)((eos - bos) < C ? (eos - bos) : C), h, vt, lane);
 
     Tout *out = static_cast<Tout *>(a.out);
-    uint32_t load_parity = 0;
+    uint32_t load_parity = 0, mma_parity = 0;
     bool failed = false;
 
     for (int64_t t0 = bos; t0 < eos; t0 += C) {
         const int len = (int)((eos - t0) < C ? (eos - t0) : C);
         cp_async_wait_all();
-        if (!mbar_wait(mbar, load_parity)) {
-            // the chunk's copies did not land within the wait bound: stop, and mark
-            // this CTA's outputs as invalid (NaN) below instead of hanging
-            failed = true;
-        }
+        if (!mbar_wait(mbar, load_parity)) failed = true;   // loads did not land: stop
         load_parity ^= 1u;
         if (!failed && len < C) zero_tail_rows(sm, len, tid);
         if (__syncthreads_or(failed)) { failed = true; break; }
+        tc_fence_after();
         if (tid == 0) *flag = 0;
 
         // ---------------- P1: in-chunk gate cumsum, exp2 space; thread = (channel pair, 8-row group E)
@@ -454,11 +586,9 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
         for (int u = 1; u < 8; ++u) { gx[u].x += gx[u - 1].x; gx[u].y += gx[u - 1].y; }
         *reinterpret_cast<float2 *>(tot8 + pE * KD + pc0) = gx[7];
         *reinterpret_cast<float2 *>(first8 + pE * KD + pc0) = gx[0];
-        for (int e = tid; e < C * VT; e += kThreads) {
-            const int r = e >> 5, j = e & 31;
-            vs[r * LDV + j] = __bfloat162float(vraw[r * VT + j]);
-        }
-        if (tid < C) beta_s[tid] = braw[tid];
+        if (tid < C * VT * 2 / 16)   // copy v (4 KB) out of the raw buffer, 16 B per thread
+            reinterpret_cast<uint4 *>(vs)[tid] = reinterpret_cast<const uint4 *>(sm + Smem::v_raw)[tid];
+        if (tid < C) beta_s[tid] = tid < len ? braw[tid * 4 + (maps.beta_tma ? (h & 3) : 0)] : 0.f;
         __syncthreads();
 
         // ---------------- P2: per-block references, scalars, factors and fp16 operands
@@ -479,24 +609,25 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
             float2 mR = mAll[0];
 #pragma unroll
             for (int R = 1; R < 4; ++R) if (R == (pE >> 1)) mR = mAll[R];
-            if (pE < 4) {   // per-block scalars of block R = pE, two channels
-                const int R = pE;
+            if (pE >= 4) {   // pair factors of block R = pE - 4, two channels
+                const int R = pE & 3;
                 float2 m = mAll[0];
 #pragma unroll
                 for (int RR = 1; RR < 4; ++RR) if (RR == R) m = mAll[RR];
-                *reinterpret_cast<uint32_t *>(pmh + R * KD + pc0) = pack_h2(exp2f(m.x), exp2f(m.y));
-                *reinterpret_cast<uint32_t *>(fmh + R * KD + pc0) =
-                    pack_h2(exp2f(glast.x - m.x), exp2f(glast.y - m.y));
 #pragma unroll
                 for (int I = 0; I < 3; ++I)
                     if (I < R)
                         *reinterpret_cast<uint32_t *>(rho + (R * (R - 1) / 2 + I) * KD + pc0) =
                             pack_h2(exp2f(m.x - mAll[I].x), exp2f(m.y - mAll[I].y));
-                if (R == 0)
-                    *reinterpret_cast<float2 *>(dec + pc0) = make_float2(exp2f(glast.x), exp2f(glast.y));
+            } else if (pE == 0) {
+                *reinterpret_cast<float2 *>(dec + pc0) = make_float2(exp2f(glast.x), exp2f(glast.y));
             }
+            // this block's scales 2^m_R (for K~, Q~) and 2^(G_last - m_R) (for K^)
+            const float pmx = exp2f(mR.x), pmy = exp2f(mR.y);
+            const float fmx = exp2f(glast.x - mR.x), fmy = exp2f(glast.y - mR.y);
             const float bx = pre.x - mR.x, by = pre.y - mR.y;   // G_r - m_R = gx + b
             bool bad = false;
+            float khx[8], khy[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int r = 8 * pE + u;
@@ -506,14 +637,35 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
                 const float epx = recip_nr(emx), epy = recip_nr(emy);
                 const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(kraw + r * KD + pc0));
                 const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qraw + r * KD + pc0));
-                *reinterpret_cast<uint32_t *>(ak + r * LD128 + pc0) = pack_h2(kv.x * emx, kv.y * emy);
-                *reinterpret_cast<uint32_t *>(aq + r * LD128 + pc0) = pack_h2(qv.x * emx, qv.y * emy);
-                *reinterpret_cast<uint32_t *>(bk + r * LD128 + pc0) = pack_h2(kv.x * epx, kv.y * epy);
+                const float akx = kv.x * emx, aky = kv.y * emy, aqx = qv.x * emx, aqy = qv.y * emy;
+                const float bkx = kv.x * epx, bky = kv.y * epy;
+                *reinterpret_cast<uint32_t *>(ak + r * LD128 + pc0) = pack_h2(akx, aky);
+                *reinterpret_cast<uint32_t *>(aq + r * LD128 + pc0) = pack_h2(aqx, aqy);
+                *reinterpret_cast<uint32_t *>(bk + r * LD128 + pc0) = pack_h2(bkx, bky);
+                *reinterpret_cast<uint32_t *>(a1 + sw128(r, pc0, 2 * C)) = pack_h2(-akx * pmx, -aky * pmy);
+                *reinterpret_cast<uint32_t *>(a1 + sw128(C + r, pc0, 2 * C)) = pack_h2(aqx * pmx, aqy * pmy);
+                khx[u] = bkx * fmx;
+                khy[u] = bky * fmy;
             }
+            // K^^T: the eight rows of this group are one 16-byte chunk of key-channel row c
+            *reinterpret_cast<uint4 *>(kht + sw128(pc0, 8 * pE, KD)) =
+                make_uint4(pack_h2(khx[0], khx[1]), pack_h2(khx[2], khx[3]),
+                           pack_h2(khx[4], khx[5]), pack_h2(khx[6], khx[7]));
+            *reinterpret_cast<uint4 *>(kht + sw128(pc0 + 1, 8 * pE, KD)) =
+                make_uint4(pack_h2(khy[0], khy[1]), pack_h2(khy[2], khy[3]),
+                           pack_h2(khy[4], khy[5]), pack_h2(khy[6], khy[7]));
             if (__any_sync(0xffffffffu, bad) && lane == 0) *flag = 1;
         }
         __syncthreads();
         const bool exact_path = *flag != 0;
+
+        // The raw buffers are free once P2 has read them, except on the exact path,
+        // which reads them during P3: the load warp fetches the next chunk now (or,
+        // on the exact path, after P3) so the copies overlap the rest of this chunk.
+        if (warp == kLoadWarp && !exact_path && t0 + C < eos) {
+            const int64_t t1 = t0 + C;
+            issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, lane);
+        }
 
         // ---------------- P3: A_kk and A_qk (lower block triangle) on tensor cores
         // Ten tasks, one 16x16 block (R, I <= R) each, both matrices per task (the B
@@ -554,10 +706,10 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
                         const int r = 16 * R + g8 + 8 * hh;
                         const int i = 16 * I + 8 * t + 2 * tig;
                         const float k0 = acc[0][t][2 * hh], k1 = acc[0][t][2 * hh + 1];
-                        akk[r * LDA + i] = (i < r) ? beta_s[r] * k0 : 0.f;
-                        akk[r * LDA + i + 1] = (i + 1 < r) ? beta_s[r] * k1 : 0.f;
+                        *reinterpret_cast<uint32_t *>(akh + sw128(r, i, C)) =
+                            pack_h2(i < r ? beta_s[r] * k0 : 0.f, i + 1 < r ? beta_s[r] * k1 : 0.f);
                         const float q0 = acc[1][t][2 * hh], q1 = acc[1][t][2 * hh + 1];
-                        *reinterpret_cast<uint32_t *>(aqk + r * LD64 + i) =
+                        *reinterpret_cast<uint32_t *>(aqk + sw128(r, i, C)) =
                             pack_h2(i <= r ? q0 : 0.f, i + 1 <= r ? q1 : 0.f);
                     }
                 }
@@ -565,19 +717,31 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
             } else if (warp < 14) {
                 const int R = warp - 10;
                 named_bar_sync(1 + R, 64);
-                invert_diag_block(akk, tmh, R, lane);
+                invert_diag_block(akh, tmh, R, lane);
             }
         } else {
             exact_intra_chunk(sm, tid);
             __syncthreads();
-            if (warp >= 10 && warp < 14) invert_diag_block(akk, tmh, warp - 10, lane);
+            if (warp >= 10 && warp < 14) invert_diag_block(akh, tmh, warp - 10, lane);
         }
+        fence_proxy_async_smem();   // A_qk, -K~/Q~ and K^^T are read by tcgen05 below
         __syncthreads();
 
-        // raw buffers are free: fetch the next chunk while the solve and state step run
-        if (t0 + C < eos) {
+        // exact path: the raw buffers are free now (the solve's barriers below are
+        // named, without the load warp)
+        if (warp == kLoadWarp && exact_path && t0 + C < eos) {
             const int64_t t1 = t0 + C;
-            issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, tid);
+            issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, lane);
+        }
+
+        // ---------------- S1 issue: D1 = [-K~; Q~] h  (X part in rows 0..63, o part in 64..127)
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < KD / 16; ++ks)
+                umma_f16(tD1, sw128_kdesc(smem_u32(a1), ks, 2 * C), sw128_kdesc(smem_u32(ht), ks, VT),
+                         kIdescM128N32, ks > 0);
+            umma_commit(mbar_mma);
         }
 
         // ---------------- P4: T = (I + A_kk)^-1 in 16x16 blocks
@@ -587,17 +751,8 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
         // on tensor cores, evaluated transposed (X^T = sum T_JI^T A_RJ^T, then
         // T_RI^T = -X^T T_RR^T) so X^T passes from accumulator to operand in registers.
         {
-            __half *akh = reinterpret_cast<__half *>(sm + Smem::xt);   // A_kk fp16 [64][LD64]
-            for (int e = tid; e < 6 * 128; e += kThreads) {            // 6 blocks x 16 rows x 8 pairs
-                const int blk = e >> 7, rem = e & 127, rr = rem >> 3, pp = (rem & 7) * 2;
-                const int R = blk == 0 ? 1 : blk < 3 ? 2 : 3;
-                const int J = blk - (R == 1 ? 0 : R == 2 ? 1 : 3);
-                const int r = 16 * R + rr, m = 16 * J + pp;
-                *reinterpret_cast<uint32_t *>(akh + r * LD64 + m) =
-                    pack_h2(akk[r * LDA + m], akk[r * LDA + m + 1]);
-            }
-            __syncthreads();
-            for (int lvl = 1; lvl < 4; ++lvl) {
+            constexpr int kSolveThreads = kThreads - 32;   // all warps but the load warp
+            for (int lvl = 1; lvl < 4 && warp != kLoadWarp; ++lvl) {
                 if (warp < 4 - lvl) {
                     const int I = warp, R = warp + lvl;
                     float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -607,8 +762,10 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
                         ldsm_x4_t(smem_u32(tmh + (16 * J + (lane & 7) + ((lane >> 4) << 3)) * LD64 +
                                            16 * I + (((lane >> 3) & 1) << 3)),
                                   af[0], af[1], af[2], af[3]);
-                        // B = A_RJ^T as [k=m][n=r] from A_RJ stored [r][m]
-                        ldsm_x4(smem_u32(akh + bnk_off(lane, 16 * R, 16 * J, LD64)), bf[0], bf[1], bf[2], bf[3]);
+                        // B = A_RJ^T as [k=m][n=r] from A_RJ stored (swizzled) [r][m]
+                        const int bn = 16 * R + (lane & 7) + ((lane >> 4) << 3);
+                        const int bkk = 16 * J + (((lane >> 3) & 1) << 3);
+                        ldsm_x4(smem_u32(akh + sw128(bn, bkk, C)), bf[0], bf[1], bf[2], bf[3]);
                         mma16816(xa[0], af, bf[0], bf[1]);
                         mma16816(xa[1], af, bf[2], bf[3]);
                     }
@@ -628,48 +785,49 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
                             tmh[r * LD64 + i] = __float2half_rn(ta[nt][e]);
                         }
                 }
-                __syncthreads();
+                named_bar_sync(5, kSolveThreads);
             }
         }
 
-        // ---------------- S1: X^T = V^T - h^T K~^T,  O1^T = h^T Q~^T   (rows v of mt, cols r of qw)
-        float xacc[4], oacc[4];
+        // ---------------- S1: decay the state for this chunk, then X = V - K~ h from D1
+        if (state_warp) {   // h <- Diag(2^G_last) h  (before K^^T D is accumulated into it)
+            tc_fence_after();
+            float hv[16];
+            tmem_ld16(tH + lane_off + 16 * hc, hv);
+            const float d = dec[sc];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int v = 16 * mt + g8 + ((e >> 1) << 3);
-            const int r = 8 * qw + 2 * tig + (e & 1);
-            xacc[e] = vs[r * LDV + v];
-            oacc[e] = 0.f;
+            for (int v = 0; v < 16; ++v) hv[v] *= d;
+            tmem_st16(tH + lane_off + 16 * hc, hv);
+            tc_fence_before();
         }
-        {
-            // B fragments: K~ = a_k 2^m_R and Q~ = a_q 2^m_R, scaled in registers (fp16)
-            const int brow = (8 * qw + (lane & 7)) * LD128 + (((lane >> 3) & 1) << 3);
-            const __half *pmr = pmh + (qw >> 1) * KD + 2 * tig;
+        if (!mbar_wait(mbar_mma, mma_parity)) failed = true;
+        mma_parity ^= 1u;
+        tc_fence_after();
+        if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {   // rows 0..63 of D1: -K~ h
+            const int r = 32 * (warp & 1) + lane, half = warp >> 2;
+            float xv[16];
+            tmem_ld16(tD1 + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, xv);
+            const float b = beta_s[r];
+            const uint4 *vrow = reinterpret_cast<const uint4 *>(vs + r * VT + 16 * half);
 #pragma unroll
-            for (int ks = 0; ks < KD / 16; ++ks) {
-                uint32_t af[4], bx[2], bq[2];
-                ldsm_x4(smem_u32(ht + a_off(lane, 16 * mt, 16 * ks, LD128)), af[0], af[1], af[2], af[3]);
-                ldsm_x2(smem_u32(ak + brow + 16 * ks), bx[0], bx[1]);
-                ldsm_x2(smem_u32(aq + brow + 16 * ks), bq[0], bq[1]);
-                const uint32_t s0 = *reinterpret_cast<const uint32_t *>(pmr + 16 * ks);
-                const uint32_t s1 = *reinterpret_cast<const uint32_t *>(pmr + 16 * ks + 8);
-                const uint32_t n0 = s0 ^ 0x80008000u, n1 = s1 ^ 0x80008000u;   // -2^m_R
-                mma16816(xacc, af, hmul2_u32(bx[0], n0), hmul2_u32(bx[1], n1));
-                mma16816(oacc, af, hmul2_u32(bq[0], s0), hmul2_u32(bq[1], s1));
+            for (int j = 0; j < 2; ++j) {
+                const uint4 w = vrow[j];
+                const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&w);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 vv = __bfloat1622float2(p2[u]);
+                    const int v = 8 * j + 2 * u;
+                    xt[(16 * half + v) * LD64 + r] = __float2half_rn(b * (vv.x + xv[v]));
+                    xt[(16 * half + v + 1) * LD64 + r] = __float2half_rn(b * (vv.y + xv[v + 1]));
+                }
             }
-        }
-        {
-            const int r = 8 * qw + 2 * tig;
-            const int v0 = 16 * mt + g8;
-            const float b0 = beta_s[r], b1 = beta_s[r + 1];
-            *reinterpret_cast<uint32_t *>(xt + v0 * LD64 + r) = pack_h2(b0 * xacc[0], b1 * xacc[1]);
-            *reinterpret_cast<uint32_t *>(xt + (v0 + 8) * LD64 + r) = pack_h2(b0 * xacc[2], b1 * xacc[3]);
+            tc_fence_before();
         }
         __syncthreads();
 
-        // ---------------- S2: D^T = (beta X)^T T^T  (T lower triangular: k-blocks <= qw/2)
-        const int rblk = qw >> 1;
+        // ---------------- S2: D^T = (beta X)^T T^T  (mma.sync; T lower triangular: k-blocks <= qw/2)
         {
+            const int mt = warp & 1, qw = warp >> 1, rblk = qw >> 1;
             float dacc[4] = {0.f, 0.f, 0.f, 0.f};
             const int brow = (8 * qw + (lane & 7)) * LD64 + (((lane >> 3) & 1) << 3);
             for (int ks = 0; ks <= rblk; ++ks) {
@@ -680,76 +838,68 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
             }
             const int r = 8 * qw + 2 * tig;
             const int v0 = 16 * mt + g8;
-            *reinterpret_cast<uint32_t *>(dt + v0 * LD64 + r) = pack_h2(dacc[0], dacc[1]);
-            *reinterpret_cast<uint32_t *>(dt + (v0 + 8) * LD64 + r) = pack_h2(dacc[2], dacc[3]);
+            *reinterpret_cast<uint32_t *>(dt + sw128(v0, r, VT)) = pack_h2(dacc[0], dacc[1]);
+            *reinterpret_cast<uint32_t *>(dt + sw128(v0 + 8, r, VT)) = pack_h2(dacc[2], dacc[3]);
         }
+        fence_proxy_async_smem();
         __syncthreads();
 
-        // ---------------- S3: O^T += D^T A_qk^T ; h^T <- h^T Diag(2^G_last) + D^T K^
+        // ---------------- S3: h += K^^T D ; D1[64..127] += A_qk D  (one tcgen05 batch)
+        if (tid == 0) {
+            tc_fence_after();
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int c = 16 * qw + 8 * nt + 2 * tig;
-            const float d0 = dec[c], d1 = dec[c + 1];
-            hreg[nt][0] *= d0; hreg[nt][1] *= d1; hreg[nt][2] *= d0; hreg[nt][3] *= d1;
-        }
-        {
-            const int brow = (8 * qw + (lane & 7)) * LD64 + (((lane >> 3) & 1) << 3);
+            for (int ks = 0; ks < C / 16; ++ks)
+                umma_f16(tH, sw128_kdesc(smem_u32(kht), ks, KD), sw128_kdesc(smem_u32(dt), ks, VT),
+                         kIdescM128N32, 1u);
+            // A = [A_kk (rows 0..63, lands in the consumed X rows); A_qk (rows 64..127)]
 #pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks) {
-                uint32_t af[4], bk0[4];
-                ldsm_x4(smem_u32(dt + a_off(lane, 16 * mt, 16 * ks, LD64)), af[0], af[1], af[2], af[3]);
-                if (ks <= rblk) {
-                    uint32_t ba[2];
-                    ldsm_x2(smem_u32(aqk + brow + 16 * ks), ba[0], ba[1]);
-                    mma16816(oacc, af, ba[0], ba[1]);
-                }
-                // K^ = b_k 2^(G_last - m_R), R = ks: one scale per key channel (n index)
-                ldsm_x4_t(smem_u32(bk + bkn_off(lane, 16 * ks, 16 * qw, LD128)), bk0[0], bk0[1], bk0[2], bk0[3]);
-                const __half f0 = fmh[ks * KD + 16 * qw + g8], f1 = fmh[ks * KD + 16 * qw + 8 + g8];
-                const __half2 f00 = __halves2half2(f0, f0), f11 = __halves2half2(f1, f1);
-                const uint32_t u0 = *reinterpret_cast<const uint32_t *>(&f00);
-                const uint32_t u1 = *reinterpret_cast<const uint32_t *>(&f11);
-                mma16816(hreg[0], af, hmul2_u32(bk0[0], u0), hmul2_u32(bk0[1], u0));
-                mma16816(hreg[1], af, hmul2_u32(bk0[2], u1), hmul2_u32(bk0[3], u1));
-            }
+            for (int ks = 0; ks < C / 16; ++ks)
+                umma_f16(tD1, sw128_kdesc(smem_u32(akh), ks, 2 * C), sw128_kdesc(smem_u32(dt), ks, VT),
+                         kIdescM128N32, 1u);
+            umma_commit(mbar_mma);
         }
-        // output rows of this chunk
+        if (!mbar_wait(mbar_mma, mma_parity)) failed = true;
+        mma_parity ^= 1u;
+        tc_fence_after();
+        if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {   // rows 64..127 of D1: o
+            const int r = 32 * (warp & 1) + lane, half = warp >> 2;
+            float ov[16];
+            tmem_ld16(tD1 + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, ov);
+            if (r < len) store_row16(out + ((t0 + r) * H + h) * VD + vt * VT + 16 * half, ov, a.scale);
+        }
+        if (state_warp) {   // fp16 mirror of the new state for the next chunk's S1
+            float hv[16];
+            tmem_ld16(tH + lane_off + 16 * hc, hv);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int v = 16 * mt + g8 + ((e >> 1) << 3);
-            const int r = 8 * qw + 2 * tig + (e & 1);
-            if (r < len)
-                out[((t0 + r) * H + h) * VD + vt * VT + v] = from_f32<Tout>(a.scale * oacc[e]);
+            for (int v = 0; v < 16; ++v) ht[sw128(16 * hc + v, sc, VT)] = __float2half_rn(hv[v]);
+            fence_proxy_async_smem();
         }
-        // fp16 mirror of the new state for the next chunk
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int c = 16 * qw + 8 * nt + 2 * tig;
-            const int v0 = 16 * mt + g8;
-            *reinterpret_cast<uint32_t *>(ht + v0 * LD128 + c) = pack_h2(hreg[nt][0], hreg[nt][1]);
-            *reinterpret_cast<uint32_t *>(ht + (v0 + 8) * LD128 + c) = pack_h2(hreg[nt][2], hreg[nt][3]);
-        }
-        // the next iteration's first barrier orders these writes before their reads
+        tc_fence_before();
+        if (__syncthreads_or(failed)) { failed = true; break; }
     }
 
     if (failed) {
-        // error marker: NaN state; the copies still in flight get one more bounded wait
+        // error marker: NaN state; copies or MMAs still in flight get one more bounded wait
         mbar_wait(mbar, load_parity);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) hreg[nt][e] = __int_as_float(0x7fc00000);
+        mbar_wait(mbar_mma, mma_parity);
     }
-    if (fin) {
+    if (fin && state_warp) {
+        tc_fence_after();
+        float hv[16];
+        tmem_ld16(tH + lane_off + 16 * hc, hv);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int v = 16 * mt + g8 + ((e >> 1) << 3);
-                const int c = 16 * qw + 8 * nt + 2 * tig + (e & 1);
-                fin[(int64_t)c * VD + vt * VT + v] = hreg[nt][e];
-            }
+        for (int j = 0; j < 4; ++j) {
+            float4 x = make_float4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
+            if (failed) x = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
+                                        __int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+            *reinterpret_cast<float4 *>(fin + (int64_t)sc * VD + vt * VT + 16 * hc + 4 * j) = x;
         }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" :: "r"(tmem), "r"(64) : "memory");
     }
 }
 
@@ -781,6 +931,21 @@ bool encode_map(CUtensorMap *m, const void *base, CUtensorMapDataType type, int 
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// beta [T, H] fp32 as a 2-D map, box 4 heads x 64 tokens (needs H % 4 == 0 for the
+// 16-byte row pitch)
+bool encode_map_2d(CUtensorMap *m, const float *base, int64_t T, int H)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * 4};
+    const cuuint32_t box[2] = {4u, (cuuint32_t)C};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename Tout>
 cudaError_t launch_tc_t(const PrefillArgs &a, cudaStream_t stream)
 {
@@ -794,6 +959,7 @@ cudaError_t launch_tc_t(const PrefillArgs &a, cudaStream_t stream)
             !encode_map(&maps.g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T, H, KD, KD) ||
             !encode_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, VD, VT))
             return cudaErrorInvalidValue;
+        maps.beta_tma = (H % 4 == 0) && encode_map_2d(&maps.beta, a.beta, T, H);
     }
     const int smem = Smem::total;
     cudaError_t e = cudaFuncSetAttribute(kda_prefill_tc_kernel<Tout>,
