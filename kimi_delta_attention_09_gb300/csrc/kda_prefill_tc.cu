@@ -19,25 +19,31 @@
 //
 // Numerics (checked against the fp64 oracle before this kernel was written):
 // * All tensor-core operands are fp16 (10-bit mantissa), accumulation fp32; the state
-//   and the triangular solve are fp32.  bf16 operands miss a 2e-3 relative bar by
-//   2-3x; fp16 operands meet it with ~3x margin.
-// * fp16 range is handled by factoring 2^(G_r - G_i) around a per-channel reference
-//   m_R = G at row 16R+8 of each 16-row block R:  a_r = x_r 2^(G_r - m_R(r)),
-//   b_i = k_i 2^(m_R(i) - G_i), and for an off-diagonal block pair the factor
-//   2^(m_R - m_I) <= 1 is applied to b in registers.  Every stored factor spans at
-//   most 8 steps of the gate.  A chunk whose factors leave [2^-8, 2^8] (gates below
-//   about -0.7 per step sustained over 8 steps) takes an exact-exponential CUDA-core
-//   path for its intra-chunk matrices instead; its result is the same algebra.
+//   and the diagonal blocks of the triangular solve are fp32.  bf16 operands miss a
+//   2e-3 relative bar by 2-3x; fp16 operands meet it with ~3x margin.
+// * fp16 range is handled by factoring 2^(G_r - G_i) around one per-channel reference
+//   m = (max_r G_r + min_r G_r) / 2 of the chunk:  a_r = x_r 2^(G_r - m) and
+//   b_i = k_i 2^(m - G_i), so every stored factor lies in [2^-8, 2^8] while the gate
+//   spans at most 16 (log2 units) over the chunk -- about 11 per 64 rows at the
+//   gate strength of the synthetic workloads.  A chunk with a wider span (gates below
+//   about -0.17 per step sustained over the chunk) takes an exact-exponential
+//   CUDA-core path for A_kk and A_qk instead; its result is the same algebra.
+// * The state-step product [K~; Q~] h is evaluated as [a_k; a_q] (2^m h), with the
+//   fp16 copy of the state scaled by 2^m per key channel (m capped at max G - 8, so
+//   a_r stays below 2^8 on either path).
 //
 // Mapping: one CTA (16 warps) per (sequence, head, 32-column tile of V); it walks its
 // sequence chunk by chunk.  The raw inputs of a chunk arrive as TMA tiles (issued one
-// chunk ahead by a dedicated warp).  Per chunk, the warps build the intra-chunk
-// operands (gate cumsum, factors, A_kk / A_qk with mma.sync, blocked solve), then run
-// the state step: the state tile h^T (fp32, 128 key channels x 32 values) lives in
-// tensor memory, and the two big contractions of the step are tcgen05 MMAs issued by
-// one thread -- [-K~; Q~] h (X and the inter-chunk part of o) and K^^T D accumulated
-// into the state, with A_qk D accumulated into o.  The small D = T (beta X) product
-// stays on mma.sync.  tcgen05 operands use the 128-byte-swizzled K-major layout.
+// chunk ahead by a dedicated warp).  Per chunk:
+//   P1/P2  gate cumsum, reference, factors; fp16 operands [a_k; a_q] (128 x 128),
+//          b (64 x 128) and K^^T (128 x 64) in 128-byte-swizzled K-major layout
+//   MMA A  [A_kk'; A_qk'] = [a_k; a_q] b^T on tcgen05 (M 128, N 64, K 128) into TMEM
+//   MMA S1 [K~ h; Q~ h] = [a_k; a_q] (2^m h) on tcgen05 (N 32), issued once the state
+//          warps have refreshed the scaled fp16 state copy and decayed the TMEM state
+//   epilogues: masked, beta-scaled A_kk and A_qk to fp16; X = beta (v - K~ h)
+//   solve  T = (I + A_kk)^-1: 16x16 diagonal blocks by fp32 forward substitution,
+//          the rest blockwise on mma.sync;  D = T X on mma.sync
+//   MMA S3 h += K^^T D and o-rows += A_qk D on tcgen05; o epilogue to global.
 #include <cstring>
 
 #include <cuda.h>
@@ -55,9 +61,8 @@ constexpr int KD = 128;          // key dim
 constexpr int VD = 128;          // value dim
 constexpr int VT = 32;           // value columns per CTA
 constexpr int kVTiles = VD / VT;
-constexpr int LD128 = KD + 8;    // f16 row stride (halves) of 128-column tiles: 272 B
 constexpr int LD64 = C + 8;      // f16 row stride of 64-column tiles: 144 B
-constexpr float kFactorMax = 256.f;   // fp16 factor bound (2^8) of the fast path
+constexpr float kSpanMax = 16.f; // widest in-chunk gate span (log2) of the fp16 fast path
 
 // Shared memory map (byte offsets).  SW128 tiles: 128-byte-swizzled K-major tcgen05
 // operands (1024-byte aligned); the others are padded row-major mma.sync operands.
@@ -67,36 +72,34 @@ struct Smem {
     static constexpr int g_raw = k_raw + C * KD * 2;         // f32  [64][128] raw natural-log gate
     static constexpr int v_raw = g_raw + C * KD * 4;         // bf16 [64][32]
     static constexpr int b_raw = v_raw + C * VT * 2;         // f32  [64][4] beta of heads 4*(h/4)..
-    static constexpr int a_k = b_raw + C * 4 * 4;            // f16 k 2^(G - m_R)  [64][LD128]
-    static constexpr int a_q = a_k + C * LD128 * 2;          // f16 q 2^(G - m_R)  [64][LD128]
-    static constexpr int b_k = a_q + C * LD128 * 2;          // f16 k 2^(m_R - G)  [64][LD128]
-    static constexpr int tm = b_k + C * LD128 * 2;           // f16  T  [64][LD64]
-    static constexpr int a1 = (tm + C * LD64 * 2 + 1023) / 1024 * 1024;   // SW128 [-K~; Q~] 128 x 128
-    static constexpr int kht = a1 + 2 * C * KD * 2;          // SW128 K^^T: 128 (channel) x 64 (row)
-    static constexpr int akh = kht + KD * C * 2;             // SW128 A_kk fp16 64 x 64
-    static constexpr int aqk = akh + C * C * 2;              // SW128 A_qk fp16 64 x 64 (follows akh:
-                                                             // [akh; aqk] is the 128-row A of o += A_qk D)
-    static constexpr int ht = aqk + C * C * 2;               // SW128 h^T fp16 32 (value) x 128 (channel)
-    static constexpr int dt = ht + VT * KD * 2;              // SW128 D^T fp16 32 (value) x 64 (row)
-    static constexpr int xt = dt + VT * C * 2;               // f16 (beta X)^T [32][LD64]
-    static constexpr int tot8 = dt;                          // f32 [8][128] group sums (P1/P2 only)
-    static constexpr int first8 = xt;                        // f32 [8][128] group firsts (P1/P2 only)
+    static constexpr int tm = b_raw + C * 4 * 4;             // f16  T  [64][LD64]
+    static constexpr int xt = tm + C * LD64 * 2;             // f16 (beta X)^T [32][LD64]
     static constexpr int vs = xt + VT * LD64 * 2;            // bf16 V [64][32]
     static constexpr int beta = vs + C * VT * 2;             // f32  [64]
     static constexpr int dec = beta + C * 4;                 // f32  [128] 2^G_last
-    static constexpr int rho = dec + KD * 4;                 // f16  [6][128] 2^(m_R - m_I), I < R
-    static constexpr int flag = rho + 6 * KD * 2;            // int
+    static constexpr int pm = dec + KD * 4;                  // f32  [128] 2^m
+    static constexpr int flag = pm + KD * 4;                 // int
     static constexpr int mbar = flag + 8;                    // u64 mbarrier of the chunk loads
-    static constexpr int mbar_mma = mbar + 8;                // u64 mbarrier of the tcgen05 MMAs
+    static constexpr int mbar_a = mbar + 8;                  // u64 mbarrier of the A-matrix MMA
+    static constexpr int mbar_mma = mbar_a + 8;              // u64 mbarrier of the state-step MMAs
     static constexpr int tmem = mbar_mma + 8;                // u32 tensor-memory base
-    static constexpr int total = tmem + 8;
+    static constexpr int aop = (tmem + 8 + 1023) / 1024 * 1024;   // SW128 [a_k; a_q] 128 x 128
+    static constexpr int bk = aop + 2 * C * KD * 2;          // SW128 b: 64 (row) x 128 (channel)
+    static constexpr int kht = bk + C * KD * 2;              // SW128 K^^T: 128 (channel) x 64 (row)
+    static constexpr int akh = kht + KD * C * 2;             // SW128 A_kk fp16 64 x 64
+    static constexpr int aqk = akh + C * C * 2;              // SW128 A_qk fp16 64 x 64 (follows akh:
+                                                             // [akh; aqk] is the 128-row A of o += A_qk D)
+    static constexpr int ht = aqk + C * C * 2;               // SW128 (2^m h)^T fp16 32 (value) x 128 (channel)
+    static constexpr int dt = ht + VT * KD * 2;              // SW128 D^T fp16 32 (value) x 64 (row)
+    static constexpr int tot8 = akh;                         // f32 [8][128] 8-row group sums   } P1/P2
+    static constexpr int first = akh + 8 * KD * 4;           // f32 [128] G of row 0              } only
+    static constexpr int total = dt + VT * C * 2;
 };
 static_assert(Smem::total <= 232448, "shared memory budget");
-static_assert(Smem::a1 % 1024 == 0 && Smem::kht % 1024 == 0 && Smem::akh % 1024 == 0 &&
-              Smem::aqk % 1024 == 0 && Smem::ht % 1024 == 0 && Smem::dt % 1024 == 0,
-              "SW128 tiles need 1024-byte alignment");
-static_assert(Smem::first8 + 8 * KD * 4 <= Smem::vs + C * VT * 2 && Smem::tot8 + 8 * KD * 4 <= Smem::xt,
-              "gate group sums fit in the D^T / (beta X)^T space");
+static_assert(Smem::aop % 1024 == 0 && Smem::bk % 1024 == 0 && Smem::kht % 1024 == 0 &&
+              Smem::akh % 1024 == 0 && Smem::aqk % 1024 == 0 && Smem::ht % 1024 == 0 &&
+              Smem::dt % 1024 == 0, "SW128 tiles need 1024-byte alignment");
+static_assert(Smem::first + KD * 4 <= Smem::ht, "gate group sums fit in the A_kk / A_qk space");
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -189,14 +192,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity)
     return false;
 }
 
-// 1/x for x in [2^-8, 2^8] on the FMA pipe: exponent-negating seed, then three
-// Newton-Raphson steps y <- y (2 - x y) (relative error ~1e-7, below fp16 rounding).
-__device__ __forceinline__ float recip_nr(float x)
+// 1/x on the special-function unit (approximate reciprocal, relative error ~2^-23,
+// far below the fp16 rounding of every operand it feeds)
+__device__ __forceinline__ float rcp_approx(float x)
 {
-    float y = __int_as_float(0x7EF311C3 - __float_as_int(x));
-    y = y * (2.f - x * y);
-    y = y * (2.f - x * y);
-    y = y * (2.f - x * y);
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -241,8 +242,10 @@ __device__ __forceinline__ uint64_t sw128_kdesc(uint32_t base, int ks, int rows)
     return sw128_desc(base + (uint32_t)((ks >> 2) * rows * 128 + (ks & 3) * 32));
 }
 
-// instruction descriptor: fp16 A and B (K-major), fp32 D, M = 128, N = 32
+// instruction descriptors: fp16 A and B (K-major), fp32 D, M = 128, N = 32 / 64
 constexpr uint32_t kIdescM128N32 = (1u << 4) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
+// the same with N = 64
+constexpr uint32_t kIdescM128N64 = (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
 
 __device__ __forceinline__ void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate)
@@ -300,12 +303,6 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi)
 {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
-}
-
-__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b)
-{
-    __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
-    return *reinterpret_cast<uint32_t *>(&r);
 }
 
 // ldmatrix lane addresses (element offsets) -----------------------------------
@@ -397,11 +394,12 @@ __device__ __forceinline__ void store_row16(__nv_bfloat16 *dst, const float (&v)
     }
 }
 
-// Exact-exponential intra-chunk matrices for chunks outside the fp16 factor range.
-// Recomputes the exp2-space cumsum G in place in g_raw, then writes A_kk and A_qk
-// (fp16) with one exponential per pair and channel, and the state-step operands
-// -K~, Q~ and K^^T with one exponential per element.
-__device__ void exact_intra_chunk(unsigned char *sm, int tid)
+// Exact-exponential intra-chunk matrices for chunks whose gate span leaves the fp16
+// fast path.  Recomputes the exp2-space cumsum G in place in g_raw, then writes A_kk
+// and A_qk (fp16, zeros above the diagonal) with one exponential per pair and
+// channel, and K^^T with one exponential per element (its fast-path values can
+// overflow at such spans).
+__device__ __noinline__ void exact_intra_chunk(unsigned char *sm, int tid)
 {
     const __nv_bfloat16 *qr = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::q_raw);
     const __nv_bfloat16 *kr = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::k_raw);
@@ -409,7 +407,6 @@ __device__ void exact_intra_chunk(unsigned char *sm, int tid)
     const float *beta = reinterpret_cast<const float *>(sm + Smem::beta);
     __half *akh = reinterpret_cast<__half *>(sm + Smem::akh);
     __half *aqk = reinterpret_cast<__half *>(sm + Smem::aqk);
-    __half *a1 = reinterpret_cast<__half *>(sm + Smem::a1);
     __half *kht = reinterpret_cast<__half *>(sm + Smem::kht);
     if (tid < KD) {
         float acc = 0.f;
@@ -437,35 +434,44 @@ __device__ void exact_intra_chunk(unsigned char *sm, int tid)
     for (int e = tid; e < C * KD; e += kThreads) {
         const int r = e >> 7, c = e & 127;
         const float gr = G[r * KD + c], gl = G[(C - 1) * KD + c];
-        const float kv = __bfloat162float(kr[r * KD + c]);
-        const float qv = __bfloat162float(qr[r * KD + c]);
-        const float eg = exp2f(gr);
-        a1[sw128(r, c, 2 * C)] = __float2half_rn(-kv * eg);
-        a1[sw128(C + r, c, 2 * C)] = __float2half_rn(qv * eg);
-        kht[sw128(c, r, KD)] = __float2half_rn(kv * exp2f(gl - gr));
+        kht[sw128(c, r, KD)] = __float2half_rn(__bfloat162float(kr[r * KD + c]) * exp2f(gl - gr));
     }
 }
 
-// T_RR = (I + A_RR)^-1 of one 16x16 diagonal block (fp32 forward substitution on the
-// fp16 A_kk, lane j owns column j), written to T (fp16) with its zeros and unit diagonal.
-__device__ __forceinline__ void invert_diag_block(const __half *akh, __half *tmh, int R, int lane)
+// T_RR = (I + A_RR)^-1 of the 16x16 diagonal blocks R = 2 P and 2 P + 1 by fp32
+// forward substitution on the fp16 A_kk: half-warp R % 2, lane j owns column j of
+// block R; row rr + 1 of the block is loaded (two 16-byte pieces, a broadcast read)
+// while row rr is reduced.  Written to T (fp16) with its zeros and unit diagonal.
+__device__ __forceinline__ void invert_diag_blocks(const __half *akh, __half *tmh, int P, int lane)
 {
-    const int j = lane & 15;
+    const int j = lane & 15, R = 2 * P + (lane >> 4);
     float col[16];
 #pragma unroll
     for (int m = 0; m < 16; ++m) col[m] = (m == j) ? 1.f : 0.f;
+    auto piece = [&](int rr, int hf) {
+        const int row = 16 * R + rr;
+        return *reinterpret_cast<const uint4 *>(akh + row * C + (((2 * R + hf) ^ (row & 7)) << 3));
+    };
+    uint4 n0 = piece(1, 0), n1 = piece(1, 1);
 #pragma unroll
-    for (int r = 1; r < 16; ++r) {
+    for (int rr = 1; rr < 16; ++rr) {
+        const uint4 c0 = n0, c1 = n1;
+        if (rr < 15) { n0 = piece(rr + 1, 0); n1 = piece(rr + 1, 1); }
+        float av[16];
+        const __half2 *p0 = reinterpret_cast<const __half2 *>(&c0);
+        const __half2 *p1 = reinterpret_cast<const __half2 *>(&c1);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 x0 = __half22float2(p0[u]), x1 = __half22float2(p1[u]);
+            av[2 * u] = x0.x; av[2 * u + 1] = x0.y; av[8 + 2 * u] = x1.x; av[8 + 2 * u + 1] = x1.y;
+        }
         float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < r; ++m)
-            s4[m & 3] += __half2float(akh[sw128(16 * R + r, 16 * R + m, C)]) * col[m];
-        if (j < r) col[r] = -((s4[0] + s4[1]) + (s4[2] + s4[3]));
+        for (int m = 0; m < rr; ++m) s4[m & 3] += av[m] * col[m];
+        if (j < rr) col[rr] = -((s4[0] + s4[1]) + (s4[2] + s4[3]));
     }
-    if (lane < 16) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) tmh[(16 * R + r) * LD64 + 16 * R + j] = __float2half_rn(col[r]);
-    }
+    for (int rr = 0; rr < 16; ++rr) tmh[(16 * R + rr) * LD64 + 16 * R + j] = __float2half_rn(col[rr]);
 }
 
 template <typename Tout>
@@ -484,11 +490,9 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     const __nv_bfloat16 *qraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::q_raw);
     const __nv_bfloat16 *kraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::k_raw);
     const float *braw = reinterpret_cast<const float *>(sm + Smem::b_raw);
-    __half *ak = reinterpret_cast<__half *>(sm + Smem::a_k);
-    __half *aq = reinterpret_cast<__half *>(sm + Smem::a_q);
-    __half *bk = reinterpret_cast<__half *>(sm + Smem::b_k);
     __half *tmh = reinterpret_cast<__half *>(sm + Smem::tm);
-    __half *a1 = reinterpret_cast<__half *>(sm + Smem::a1);
+    __half *aop = reinterpret_cast<__half *>(sm + Smem::aop);
+    __half *bop = reinterpret_cast<__half *>(sm + Smem::bk);
     __half *kht = reinterpret_cast<__half *>(sm + Smem::kht);
     __half *akh = reinterpret_cast<__half *>(sm + Smem::akh);
     __half *aqk = reinterpret_cast<__half *>(sm + Smem::aqk);
@@ -498,9 +502,9 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     __nv_bfloat16 *vs = reinterpret_cast<__nv_bfloat16 *>(sm + Smem::vs);
     float *beta_s = reinterpret_cast<float *>(sm + Smem::beta);
     float *dec = reinterpret_cast<float *>(sm + Smem::dec);
-    __half *rho = reinterpret_cast<__half *>(sm + Smem::rho);
+    float *pm = reinterpret_cast<float *>(sm + Smem::pm);
     float *tot8 = reinterpret_cast<float *>(sm + Smem::tot8);
-    float *first8 = reinterpret_cast<float *>(sm + Smem::first8);
+    float *first = reinterpret_cast<float *>(sm + Smem::first);
     volatile int *flag = reinterpret_cast<volatile int *>(sm + Smem::flag);
 
     int64_t bos, eos;
@@ -509,39 +513,38 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     float *fin;
     prefill_state_ptrs(a, n, h, init, fin);
 
-    // ---- tensor memory (64 columns: [0, 32) the step accumulator D1, [32, 64) the state
-    //      h^T with lane = key channel, column = value) and the two mbarriers
+    // ---- tensor memory (128 columns: [0, 32) the step accumulator D1, [32, 64) the
+    //      state h^T with lane = key channel, column = value, [64, 128) the A matrices)
+    //      and the three mbarriers
     const uint32_t mbar = smem_u32(sm + Smem::mbar);
+    const uint32_t mbar_a = smem_u32(sm + Smem::mbar_a);
     const uint32_t mbar_mma = smem_u32(sm + Smem::mbar_mma);
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
-                     :: "r"(smem_u32(sm + Smem::tmem)), "r"(64) : "memory");
+                     :: "r"(smem_u32(sm + Smem::tmem)), "r"(128) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
     if (tid == 0) {
         mbar_init(mbar, 1);
+        mbar_init(mbar_a, 1);
         mbar_init(mbar_mma, 1);
-    }
-    // A_qk blocks above the diagonal are never written by the fast path; zero them once
-    for (int e = tid; e < C * C; e += kThreads) {
-        const int r = e >> 6, i = e & 63;
-        if ((i >> 4) > (r >> 4)) aqk[sw128(r, i, C)] = __float2half_rn(0.f);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Smem::tmem);
-    const uint32_t tD1 = tmem, tH = tmem + 32;
+    const uint32_t tD1 = tmem, tH = tmem + 32, tDA = tmem + 64;
 
-    // TMEM epilogue roles (warp w reaches lanes 32 (w % 4) .. +31):
+    // TMEM roles (warp w reaches lanes 32 (w % 4) .. +31):
     //   state warps 8..15: key channels sc = 32 (w % 4) + lane, value columns [16 hc, 16 hc + 16)
+    //   A matrices (lanes 0..63 A_kk, 64..127 A_qk): warps 0..7, columns [32 (w / 4), +32)
     //   X rows (lanes 0..63): warps 0, 1 (columns 0..15) and 4, 5 (columns 16..31)
     //   o rows (lanes 64..127): warps 2, 3 (columns 0..15) and 6, 7 (columns 16..31)
     const bool state_warp = warp >= 8;
     const int sc = 32 * (warp & 3) + lane;                       // key channel of a state warp
     const int hc = (warp >> 2) & 1;                              // its half of the value columns
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // TMEM lane quadrant
-    if (state_warp) {   // initial state -> tensor memory and its fp16 mirror
+    if (state_warp) {   // initial state -> tensor memory
         float hv[16];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -550,9 +553,6 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
             hv[4 * j] = x.x; hv[4 * j + 1] = x.y; hv[4 * j + 2] = x.z; hv[4 * j + 3] = x.w;
         }
         tmem_st16(tH + lane_off + 16 * hc, hv);
-#pragma unroll
-        for (int v = 0; v < 16; ++v) ht[sw128(16 * hc + v, sc, VT)] = __float2half_rn(hv[v]);
-        fence_proxy_async_smem();
         tc_fence_before();
     }
 
@@ -561,7 +561,7 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
         issue_chunk_loads(sm, a, maps, bos, (int)((eos - bos) < C ? (eos - bos) : C), h, vt, lane);
 
     Tout *out = static_cast<Tout *>(a.out);
-    uint32_t load_parity = 0, mma_parity = 0;
+    uint32_t load_parity = 0, a_parity = 0, mma_parity = 0;
     bool failed = false;
 
     for (int64_t t0 = bos; t0 < eos; t0 += C) {
@@ -585,67 +585,48 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
 #pragma unroll
         for (int u = 1; u < 8; ++u) { gx[u].x += gx[u - 1].x; gx[u].y += gx[u - 1].y; }
         *reinterpret_cast<float2 *>(tot8 + pE * KD + pc0) = gx[7];
-        *reinterpret_cast<float2 *>(first8 + pE * KD + pc0) = gx[0];
+        if (pE == 0) *reinterpret_cast<float2 *>(first + pc0) = gx[0];
         if (tid < C * VT * 2 / 16)   // copy v (4 KB) out of the raw buffer, 16 B per thread
             reinterpret_cast<uint4 *>(vs)[tid] = reinterpret_cast<const uint4 *>(sm + Smem::v_raw)[tid];
         if (tid < C) beta_s[tid] = tid < len ? braw[tid * 4 + (maps.beta_tma ? (h & 3) : 0)] : 0.f;
         __syncthreads();
 
-        // ---------------- P2: per-block references, scalars, factors and fp16 operands
+        // ---------------- P2: reference, factors and the fp16 tcgen05 operands
         {
-            // prefix sums over the 8-row groups; block references m_R = G(row 16R+8)
-            float2 pre = make_float2(0.f, 0.f), run = make_float2(0.f, 0.f), mAll[4];
+            float2 pre = make_float2(0.f, 0.f), run = make_float2(0.f, 0.f);
 #pragma unroll
             for (int E = 0; E < 8; ++E) {
                 const float2 t = *reinterpret_cast<const float2 *>(tot8 + E * KD + pc0);
-                if (E & 1) {
-                    const float2 f = *reinterpret_cast<const float2 *>(first8 + E * KD + pc0);
-                    mAll[E >> 1] = make_float2(run.x + f.x, run.y + f.y);
-                }
                 if (E == pE) pre = run;
                 run.x += t.x; run.y += t.y;
             }
-            const float2 glast = run;
-            float2 mR = mAll[0];
-#pragma unroll
-            for (int R = 1; R < 4; ++R) if (R == (pE >> 1)) mR = mAll[R];
-            if (pE >= 4) {   // pair factors of block R = pE - 4, two channels
-                const int R = pE & 3;
-                float2 m = mAll[0];
-#pragma unroll
-                for (int RR = 1; RR < 4; ++RR) if (RR == R) m = mAll[RR];
-#pragma unroll
-                for (int I = 0; I < 3; ++I)
-                    if (I < R)
-                        *reinterpret_cast<uint32_t *>(rho + (R * (R - 1) / 2 + I) * KD + pc0) =
-                            pack_h2(exp2f(m.x - mAll[I].x), exp2f(m.y - mAll[I].y));
-            } else if (pE == 0) {
+            const float2 glast = run, g0 = *reinterpret_cast<const float2 *>(first + pc0);
+            // reference: the midpoint of the first and last row's G (the midrange when
+            // the gate is a decay), capped so that no factor 2^(G - m) exceeds 2^8 then
+            const float mx_ = fmaxf(0.5f * (g0.x + glast.x), g0.x - 0.5f * kSpanMax);
+            const float my_ = fmaxf(0.5f * (g0.y + glast.y), g0.y - 0.5f * kSpanMax);
+            if (pE == 0) {
+                *reinterpret_cast<float2 *>(pm + pc0) = make_float2(exp2f(mx_), exp2f(my_));
                 *reinterpret_cast<float2 *>(dec + pc0) = make_float2(exp2f(glast.x), exp2f(glast.y));
             }
-            // this block's scales 2^m_R (for K~, Q~) and 2^(G_last - m_R) (for K^)
-            const float pmx = exp2f(mR.x), pmy = exp2f(mR.y);
-            const float fmx = exp2f(glast.x - mR.x), fmy = exp2f(glast.y - mR.y);
-            const float bx = pre.x - mR.x, by = pre.y - mR.y;   // G_r - m_R = gx + b
-            bool bad = false;
-            float khx[8], khy[8];
+            const float fx = exp2f(glast.x - mx_), fy = exp2f(glast.y - my_);   // K^ = b 2^(G_last - m)
+            const float bx = pre.x - mx_, by = pre.y - my_;                    // G_r - m = gx + b
+            float khx[8], khy[8], amax = 0.f;
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int r = 8 * pE + u;
-                const float emx = exp2f(gx[u].x + bx), emy = exp2f(gx[u].y + by);
-                bad |= !(emx <= kFactorMax && emx >= 1.f / kFactorMax &&
-                         emy <= kFactorMax && emy >= 1.f / kFactorMax);
-                const float epx = recip_nr(emx), epy = recip_nr(emy);
+                const float xx = gx[u].x + bx, xy = gx[u].y + by;   // G_r - m
+                amax = fmaxf(amax, fmaxf(fabsf(xx), fabsf(xy)));
+                const float ex = exp2f(xx), ey = exp2f(xy);
+                const float ix = rcp_approx(ex), iy = rcp_approx(ey);
                 const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(kraw + r * KD + pc0));
                 const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qraw + r * KD + pc0));
-                const float akx = kv.x * emx, aky = kv.y * emy, aqx = qv.x * emx, aqy = qv.y * emy;
-                const float bkx = kv.x * epx, bky = kv.y * epy;
-                *reinterpret_cast<uint32_t *>(ak + r * LD128 + pc0) = pack_h2(akx, aky);
-                *reinterpret_cast<uint32_t *>(aq + r * LD128 + pc0) = pack_h2(aqx, aqy);
-                *reinterpret_cast<uint32_t *>(bk + r * LD128 + pc0) = pack_h2(bkx, bky);
-                *reinterpret_cast<uint32_t *>(a1 + sw128(r, pc0, 2 * C)) = pack_h2(-akx * pmx, -aky * pmy);
-                *reinterpret_cast<uint32_t *>(a1 + sw128(C + r, pc0, 2 * C)) = pack_h2(aqx * pmx, aqy * pmy);
-                khx[u] = bkx * fmx;
-                khy[u] = bky * fmy;
+                *reinterpret_cast<uint32_t *>(aop + sw128(r, pc0, 2 * C)) = pack_h2(kv.x * ex, kv.y * ey);
+                *reinterpret_cast<uint32_t *>(aop + sw128(C + r, pc0, 2 * C)) = pack_h2(qv.x * ex, qv.y * ey);
+                const float b0 = kv.x * ix, b1 = kv.y * iy;
+                *reinterpret_cast<uint32_t *>(bop + sw128(r, pc0, C)) = pack_h2(b0, b1);
+                khx[u] = b0 * fx;
+                khy[u] = b1 * fy;
             }
             // K^^T: the eight rows of this group are one 16-byte chunk of key-channel row c
             *reinterpret_cast<uint4 *>(kht + sw128(pc0, 8 * pE, KD)) =
@@ -654,156 +635,102 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
             *reinterpret_cast<uint4 *>(kht + sw128(pc0 + 1, 8 * pE, KD)) =
                 make_uint4(pack_h2(khy[0], khy[1]), pack_h2(khy[2], khy[3]),
                            pack_h2(khy[4], khy[5]), pack_h2(khy[6], khy[7]));
-            if (__any_sync(0xffffffffu, bad) && lane == 0) *flag = 1;
+            // fast path: every factor 2^(G_r - m) within [2^-8, 2^8]
+            if (__any_sync(0xffffffffu, !(amax <= 0.5f * kSpanMax)) && lane == 0) *flag = 1;
+            fence_proxy_async_smem();   // the operands are read by tcgen05 below
         }
         __syncthreads();
         const bool exact_path = *flag != 0;
 
+        // ---------------- MMA A: [A_kk'; A_qk'] = [a_k; a_q] b^T  (fast path)
+        if (!exact_path && tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < KD / 16; ++ks)
+                umma_f16(tDA, sw128_kdesc(smem_u32(aop), ks, 2 * C), sw128_kdesc(smem_u32(bop), ks, C),
+                         kIdescM128N64, ks > 0);
+            umma_commit(mbar_a);
+        }
         // The raw buffers are free once P2 has read them, except on the exact path,
-        // which reads them during P3: the load warp fetches the next chunk now (or,
-        // on the exact path, after P3) so the copies overlap the rest of this chunk.
+        // which reads them below: the load warp fetches the next chunk now (or, on the
+        // exact path, after the intra-chunk matrices) so the copies overlap the rest.
         if (warp == kLoadWarp && !exact_path && t0 + C < eos) {
             const int64_t t1 = t0 + C;
             issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, lane);
         }
-
-        // ---------------- P3: A_kk and A_qk (lower block triangle) on tensor cores
-        // Ten tasks, one 16x16 block (R, I <= R) each, both matrices per task (the B
-        // fragments of block I serve A_kk and A_qk); warp w % 4 picks the scheduler, so
-        // the tasks are placed three, three, two and two per scheduler.  Warps 10..13
-        // invert the diagonal blocks as soon as the task that owns them has stored them.
-        if (!exact_path) {
-            if (warp < 10) {
-                const int R = warp < 4 ? 3 : warp < 7 ? 2 : warp < 9 ? 1 : 0;
-                const int I = warp < 4 ? warp : warp < 7 ? warp - 4 : warp < 9 ? warp - 7 : 0;
-                float acc[2][2][4];   // [matrix][n8 tile][frag]
+        // ---------------- state warps: fp16 copy (2^m h)^T for S1, then h <- Diag(2^G_last) h
+        constexpr int kS1Bar = 6, kS1Threads = 9 * 32;   // state warps + warp 0
+        if (state_warp) {
+            tc_fence_after();
+            float hv[16];
+            tmem_ld16(tH + lane_off + 16 * hc, hv);
+            const float p = pm[sc], d = dec[sc];
 #pragma unroll
-                for (int m = 0; m < 2; ++m)
-#pragma unroll
-                    for (int t = 0; t < 2; ++t) acc[m][t][0] = acc[m][t][1] = acc[m][t][2] = acc[m][t][3] = 0.f;
-                const __half *rp = rho + (I < R ? R * (R - 1) / 2 + I : 0) * KD + 2 * tig;
-#pragma unroll
-                for (int ks = 0; ks < KD / 16; ++ks) {
-                    uint32_t fk[4], fq[4], bf[4];
-                    ldsm_x4(smem_u32(ak + a_off(lane, 16 * R, 16 * ks, LD128)), fk[0], fk[1], fk[2], fk[3]);
-                    ldsm_x4(smem_u32(aq + a_off(lane, 16 * R, 16 * ks, LD128)), fq[0], fq[1], fq[2], fq[3]);
-                    ldsm_x4(smem_u32(bk + bnk_off(lane, 16 * I, 16 * ks, LD128)), bf[0], bf[1], bf[2], bf[3]);
-                    if (I < R) {
-                        const uint32_t s0 = *reinterpret_cast<const uint32_t *>(rp + 16 * ks);
-                        const uint32_t s1 = *reinterpret_cast<const uint32_t *>(rp + 16 * ks + 8);
-                        bf[0] = hmul2_u32(bf[0], s0); bf[1] = hmul2_u32(bf[1], s1);
-                        bf[2] = hmul2_u32(bf[2], s0); bf[3] = hmul2_u32(bf[3], s1);
-                    }
-                    mma16816(acc[0][0], fk, bf[0], bf[1]);
-                    mma16816(acc[0][1], fk, bf[2], bf[3]);
-                    mma16816(acc[1][0], fq, bf[0], bf[1]);
-                    mma16816(acc[1][1], fq, bf[2], bf[3]);
-                }
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int r = 16 * R + g8 + 8 * hh;
-                        const int i = 16 * I + 8 * t + 2 * tig;
-                        const float k0 = acc[0][t][2 * hh], k1 = acc[0][t][2 * hh + 1];
-                        *reinterpret_cast<uint32_t *>(akh + sw128(r, i, C)) =
-                            pack_h2(i < r ? beta_s[r] * k0 : 0.f, i + 1 < r ? beta_s[r] * k1 : 0.f);
-                        const float q0 = acc[1][t][2 * hh], q1 = acc[1][t][2 * hh + 1];
-                        *reinterpret_cast<uint32_t *>(aqk + sw128(r, i, C)) =
-                            pack_h2(i <= r ? q0 : 0.f, i + 1 <= r ? q1 : 0.f);
-                    }
-                }
-                if (I == R) named_bar_arrive(1 + R, 64);   // diagonal block stored
-            } else if (warp < 14) {
-                const int R = warp - 10;
-                named_bar_sync(1 + R, 64);
-                invert_diag_block(akh, tmh, R, lane);
+            for (int v = 0; v < 16; ++v) {
+                ht[sw128(16 * hc + v, sc, VT)] = __float2half_rn(p * hv[v]);
+                hv[v] *= d;
             }
+            tmem_st16(tH + lane_off + 16 * hc, hv);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar_arrive(kS1Bar, kS1Threads);
+        } else if (warp == 0) {
+            named_bar_sync(kS1Bar, kS1Threads);
+            // ---------------- MMA S1: D1 = [a_k; a_q] (2^m h) = [K~ h; Q~ h]
+            if (tid == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < KD / 16; ++ks)
+                    umma_f16(tD1, sw128_kdesc(smem_u32(aop), ks, 2 * C), sw128_kdesc(smem_u32(ht), ks, VT),
+                             kIdescM128N32, ks > 0);
+                umma_commit(mbar_mma);
+            }
+        }
+
+        // ---------------- A epilogue: masked, beta-scaled fp16 A_kk and A_qk
+        if (!exact_path) {
+            if (warp < 8) {
+                if (!mbar_wait(mbar_a, a_parity)) failed = true;
+                tc_fence_after();
+                const int c0 = 32 * (warp >> 2), rg = 32 * (warp & 3) + lane;
+                float av[2][16];
+                tmem_ld16(tDA + ((uint32_t)(32 * (warp & 3)) << 16) + c0, av[0]);
+                tmem_ld16(tDA + ((uint32_t)(32 * (warp & 3)) << 16) + c0 + 16, av[1]);
+                const bool kk = rg < C;
+                const int r = kk ? rg : rg - C;
+                const float sb = kk ? beta_s[r] : 1.f;
+                const int lim = kk ? r : r + 1;   // columns i < lim are kept
+                __half *dst = kk ? akh : aqk;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int e = 8 * t + 2 * u, i = c0 + e;
+                        const float x0 = i < lim ? sb * av[e >> 4][e & 15] : 0.f;
+                        const float x1 = i + 1 < lim ? sb * av[(e + 1) >> 4][(e + 1) & 15] : 0.f;
+                        w[u] = pack_h2(x0, x1);
+                    }
+                    *reinterpret_cast<uint4 *>(dst + sw128(r, c0 + 8 * t, C)) = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                tc_fence_before();
+            }
+            a_parity ^= 1u;
         } else {
             exact_intra_chunk(sm, tid);
-            __syncthreads();
-            if (warp >= 10 && warp < 14) invert_diag_block(akh, tmh, warp - 10, lane);
         }
-        fence_proxy_async_smem();   // A_qk, -K~/Q~ and K^^T are read by tcgen05 below
+        fence_proxy_async_smem();   // A_qk, A_kk and K^^T are read by tcgen05 below
         __syncthreads();
-
-        // exact path: the raw buffers are free now (the solve's barriers below are
-        // named, without the load warp)
         if (warp == kLoadWarp && exact_path && t0 + C < eos) {
             const int64_t t1 = t0 + C;
             issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, lane);
         }
 
-        // ---------------- S1 issue: D1 = [-K~; Q~] h  (X part in rows 0..63, o part in 64..127)
-        if (tid == 0) {
+        // ---------------- diagonal blocks of T (warps 10, 11) || X = beta (v - K~ h) (warps 0, 1, 4, 5)
+        if (warp == 10 || warp == 11) invert_diag_blocks(akh, tmh, warp - 10, lane);
+        if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {   // rows 0..63 of D1: K~ h
+            if (!mbar_wait(mbar_mma, mma_parity)) failed = true;
             tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < KD / 16; ++ks)
-                umma_f16(tD1, sw128_kdesc(smem_u32(a1), ks, 2 * C), sw128_kdesc(smem_u32(ht), ks, VT),
-                         kIdescM128N32, ks > 0);
-            umma_commit(mbar_mma);
-        }
-
-        // ---------------- P4: T = (I + A_kk)^-1 in 16x16 blocks
-        // Diagonal blocks were inverted during P3.  Below-diagonal blocks, by distance
-        // from the diagonal:
-        //     T_RI = -T_RR sum_{J=I}^{R-1} A_RJ T_JI
-        // on tensor cores, evaluated transposed (X^T = sum T_JI^T A_RJ^T, then
-        // T_RI^T = -X^T T_RR^T) so X^T passes from accumulator to operand in registers.
-        {
-            constexpr int kSolveThreads = kThreads - 32;   // all warps but the load warp
-            for (int lvl = 1; lvl < 4 && warp != kLoadWarp; ++lvl) {
-                if (warp < 4 - lvl) {
-                    const int I = warp, R = warp + lvl;
-                    float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    for (int J = I; J < R; ++J) {
-                        uint32_t af[4], bf[4];
-                        // A = T_JI^T (rows i, cols m) from T_JI stored [m][i]
-                        ldsm_x4_t(smem_u32(tmh + (16 * J + (lane & 7) + ((lane >> 4) << 3)) * LD64 +
-                                           16 * I + (((lane >> 3) & 1) << 3)),
-                                  af[0], af[1], af[2], af[3]);
-                        // B = A_RJ^T as [k=m][n=r] from A_RJ stored (swizzled) [r][m]
-                        const int bn = 16 * R + (lane & 7) + ((lane >> 4) << 3);
-                        const int bkk = 16 * J + (((lane >> 3) & 1) << 3);
-                        ldsm_x4(smem_u32(akh + sw128(bn, bkk, C)), bf[0], bf[1], bf[2], bf[3]);
-                        mma16816(xa[0], af, bf[0], bf[1]);
-                        mma16816(xa[1], af, bf[2], bf[3]);
-                    }
-                    const uint32_t xf[4] = {pack_h2(-xa[0][0], -xa[0][1]), pack_h2(-xa[0][2], -xa[0][3]),
-                                            pack_h2(-xa[1][0], -xa[1][1]), pack_h2(-xa[1][2], -xa[1][3])};
-                    uint32_t tb[4];
-                    ldsm_x4(smem_u32(tmh + bnk_off(lane, 16 * R, 16 * R, LD64)), tb[0], tb[1], tb[2], tb[3]);
-                    float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                    mma16816(ta[0], xf, tb[0], tb[1]);
-                    mma16816(ta[1], xf, tb[2], tb[3]);
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i = 16 * I + g8 + ((e >> 1) << 3);
-                            const int r = 16 * R + 8 * nt + 2 * tig + (e & 1);
-                            tmh[r * LD64 + i] = __float2half_rn(ta[nt][e]);
-                        }
-                }
-                named_bar_sync(5, kSolveThreads);
-            }
-        }
-
-        // ---------------- S1: decay the state for this chunk, then X = V - K~ h from D1
-        if (state_warp) {   // h <- Diag(2^G_last) h  (before K^^T D is accumulated into it)
-            tc_fence_after();
-            float hv[16];
-            tmem_ld16(tH + lane_off + 16 * hc, hv);
-            const float d = dec[sc];
-#pragma unroll
-            for (int v = 0; v < 16; ++v) hv[v] *= d;
-            tmem_st16(tH + lane_off + 16 * hc, hv);
-            tc_fence_before();
-        }
-        if (!mbar_wait(mbar_mma, mma_parity)) failed = true;
-        mma_parity ^= 1u;
-        tc_fence_after();
-        if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {   // rows 0..63 of D1: -K~ h
             const int r = 32 * (warp & 1) + lane, half = warp >> 2;
             float xv[16];
             tmem_ld16(tD1 + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, xv);
@@ -817,13 +744,55 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
                 for (int u = 0; u < 4; ++u) {
                     const float2 vv = __bfloat1622float2(p2[u]);
                     const int v = 8 * j + 2 * u;
-                    xt[(16 * half + v) * LD64 + r] = __float2half_rn(b * (vv.x + xv[v]));
-                    xt[(16 * half + v + 1) * LD64 + r] = __float2half_rn(b * (vv.y + xv[v + 1]));
+                    xt[(16 * half + v) * LD64 + r] = __float2half_rn(b * (vv.x - xv[v]));
+                    xt[(16 * half + v + 1) * LD64 + r] = __float2half_rn(b * (vv.y - xv[v + 1]));
                 }
             }
             tc_fence_before();
         }
+        mma_parity ^= 1u;
         __syncthreads();
+
+        // ---------------- T below the diagonal blocks, by distance from the diagonal:
+        //     T_RI = -T_RR sum_{J=I}^{R-1} A_RJ T_JI
+        // on tensor cores, evaluated transposed (X^T = sum T_JI^T A_RJ^T, then
+        // T_RI^T = -X^T T_RR^T) so X^T passes from accumulator to operand in registers.
+#pragma unroll 1
+        for (int lvl = 1; lvl < 4; ++lvl) {
+            if (warp < 4 - lvl) {
+                const int I = warp, R = warp + lvl;
+                float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                for (int J = I; J < R; ++J) {
+                    uint32_t af[4], bf[4];
+                    // A = T_JI^T (rows i, cols m) from T_JI stored [m][i]
+                    ldsm_x4_t(smem_u32(tmh + (16 * J + (lane & 7) + ((lane >> 4) << 3)) * LD64 +
+                                       16 * I + (((lane >> 3) & 1) << 3)),
+                              af[0], af[1], af[2], af[3]);
+                    // B = A_RJ^T as [k=m][n=r] from A_RJ stored (swizzled) [r][m]
+                    const int bn = 16 * R + (lane & 7) + ((lane >> 4) << 3);
+                    const int bkk = 16 * J + (((lane >> 3) & 1) << 3);
+                    ldsm_x4(smem_u32(akh + sw128(bn, bkk, C)), bf[0], bf[1], bf[2], bf[3]);
+                    mma16816(xa[0], af, bf[0], bf[1]);
+                    mma16816(xa[1], af, bf[2], bf[3]);
+                }
+                const uint32_t xf[4] = {pack_h2(-xa[0][0], -xa[0][1]), pack_h2(-xa[0][2], -xa[0][3]),
+                                        pack_h2(-xa[1][0], -xa[1][1]), pack_h2(-xa[1][2], -xa[1][3])};
+                uint32_t tb[4];
+                ldsm_x4(smem_u32(tmh + bnk_off(lane, 16 * R, 16 * R, LD64)), tb[0], tb[1], tb[2], tb[3]);
+                float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                mma16816(ta[0], xf, tb[0], tb[1]);
+                mma16816(ta[1], xf, tb[2], tb[3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = 16 * I + g8 + ((e >> 1) << 3);
+                        const int r = 16 * R + 8 * nt + 2 * tig + (e & 1);
+                        tmh[r * LD64 + i] = __float2half_rn(ta[nt][e]);
+                    }
+            }
+            __syncthreads();
+        }
 
         // ---------------- S2: D^T = (beta X)^T T^T  (mma.sync; T lower triangular: k-blocks <= qw/2)
         {
@@ -844,7 +813,7 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
         fence_proxy_async_smem();
         __syncthreads();
 
-        // ---------------- S3: h += K^^T D ; D1[64..127] += A_qk D  (one tcgen05 batch)
+        // ---------------- MMA S3: h += K^^T D ; D1[64..127] += A_qk D  (one tcgen05 batch)
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
@@ -867,13 +836,6 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
             tmem_ld16(tD1 + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, ov);
             if (r < len) store_row16(out + ((t0 + r) * H + h) * VD + vt * VT + 16 * half, ov, a.scale);
         }
-        if (state_warp) {   // fp16 mirror of the new state for the next chunk's S1
-            float hv[16];
-            tmem_ld16(tH + lane_off + 16 * hc, hv);
-#pragma unroll
-            for (int v = 0; v < 16; ++v) ht[sw128(16 * hc + v, sc, VT)] = __float2half_rn(hv[v]);
-            fence_proxy_async_smem();
-        }
         tc_fence_before();
         if (__syncthreads_or(failed)) { failed = true; break; }
     }
@@ -881,6 +843,7 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     if (failed) {
         // error marker: NaN state; copies or MMAs still in flight get one more bounded wait
         mbar_wait(mbar, load_parity);
+        mbar_wait(mbar_a, a_parity);
         mbar_wait(mbar_mma, mma_parity);
     }
     if (fin && state_warp) {
@@ -899,7 +862,7 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" :: "r"(tmem), "r"(64) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" :: "r"(tmem), "r"(128) : "memory");
     }
 }
 
