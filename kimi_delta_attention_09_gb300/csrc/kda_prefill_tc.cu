@@ -55,7 +55,10 @@
 namespace kda {
 namespace {
 
-constexpr int kThreads = 512;   // 16 warps
+constexpr int kThreads = 512;   // 16 warps: two groups of 8
+constexpr int kGroup = 256;     // threads per group
+constexpr int kBarPrep = 1;     // named barrier of the operand group (warps 8..15)
+constexpr int kBarStep = 2;     // named barrier of the state-step group (warps 0..7)
 constexpr int C = kChunk;        // 64 rows per chunk
 constexpr int KD = 128;          // key dim
 constexpr int VD = 128;          // value dim
@@ -66,40 +69,44 @@ constexpr float kSpanMax = 16.f; // widest in-chunk gate span (log2) of the fp16
 
 // Shared memory map (byte offsets).  SW128 tiles: 128-byte-swizzled K-major tcgen05
 // operands (1024-byte aligned); the others are padded row-major mma.sync operands.
+// "x2" buffers are double-buffered by chunk parity: the operand group fills slot
+// n % 2 for chunk n while the state-step group still reads slot (n - 1) % 2.
 struct Smem {
     static constexpr int q_raw = 0;                          // bf16 [64][128]
     static constexpr int k_raw = q_raw + C * KD * 2;         // bf16 [64][128]
     static constexpr int g_raw = k_raw + C * KD * 2;         // f32  [64][128] raw natural-log gate
     static constexpr int v_raw = g_raw + C * KD * 4;         // bf16 [64][32]
     static constexpr int b_raw = v_raw + C * VT * 2;         // f32  [64][4] beta of heads 4*(h/4)..
-    static constexpr int tm = b_raw + C * 4 * 4;             // f16  T  [64][LD64]
-    static constexpr int xt = tm + C * LD64 * 2;             // f16 (beta X)^T [32][LD64]
-    static constexpr int vs = xt + VT * LD64 * 2;            // bf16 V [64][32]
-    static constexpr int beta = vs + C * VT * 2;             // f32  [64]
-    static constexpr int dec = beta + C * 4;                 // f32  [128] 2^G_last
-    static constexpr int pm = dec + KD * 4;                  // f32  [128] 2^m
-    static constexpr int flag = pm + KD * 4;                 // int
-    static constexpr int mbar = flag + 8;                    // u64 mbarrier of the chunk loads
-    static constexpr int mbar_a = mbar + 8;                  // u64 mbarrier of the A-matrix MMA
-    static constexpr int mbar_mma = mbar_a + 8;              // u64 mbarrier of the state-step MMAs
-    static constexpr int tmem = mbar_mma + 8;                // u32 tensor-memory base
-    static constexpr int aop = (tmem + 8 + 1023) / 1024 * 1024;   // SW128 [a_k; a_q] 128 x 128
+    static constexpr int tm = b_raw + C * 4 * 4;             // f16 T [64][LD64]
+    static constexpr int vs = tm + C * LD64 * 2;             // x2 bf16 V [64][32]
+    static constexpr int beta = vs + 2 * C * VT * 2;         // x2 f32 [64]
+    static constexpr int dec = beta + 2 * C * 4;             // x2 f32 [128] 2^G_last
+    static constexpr int pm = dec + 2 * KD * 4;              // x2 f32 [128] 2^m
+    static constexpr int tdg = pm + 2 * KD * 4;              // x2 f16 T_RR [4][16][16] (diagonal blocks)
+    static constexpr int bars = tdg + 2 * 4 * 16 * 16 * 2;             // u64 mbarriers (see Bar)
+    static constexpr int tmem = bars + 8 * 8;                // u32 tensor-memory base
+    static constexpr int flag = tmem + 4;                    // int: exact path for this chunk
+    static constexpr int aop = (flag + 4 + 1023) / 1024 * 1024;   // SW128 [a_k; a_q] 128 x 128
     static constexpr int bk = aop + 2 * C * KD * 2;          // SW128 b: 64 (row) x 128 (channel)
-    static constexpr int kht = bk + C * KD * 2;              // SW128 K^^T: 128 (channel) x 64 (row)
-    static constexpr int akh = kht + KD * C * 2;             // SW128 A_kk fp16 64 x 64
-    static constexpr int aqk = akh + C * C * 2;              // SW128 A_qk fp16 64 x 64 (follows akh:
-                                                             // [akh; aqk] is the 128-row A of o += A_qk D)
-    static constexpr int ht = aqk + C * C * 2;               // SW128 (2^m h)^T fp16 32 (value) x 128 (channel)
+    static constexpr int kht = bk + C * KD * 2;              // x2 SW128 K^^T: 128 (channel) x 64 (row)
+    static constexpr int akh = kht + 2 * KD * C * 2;         // x2 [SW128 A_kk 64 x 64; SW128 A_qk 64 x 64]
+                                                             // ([A_kk; A_qk] is the 128-row A of o += A_qk D)
+    static constexpr int ht = akh + 2 * 2 * C * C * 2;       // SW128 (2^m h)^T fp16 32 (value) x 128 (channel)
+    static constexpr int xt = ht;                            // f16 (beta X)^T [32][LD64]: written once S1
+                                                             // (the only reader of ht) has completed
     static constexpr int dt = ht + VT * KD * 2;              // SW128 D^T fp16 32 (value) x 64 (row)
-    static constexpr int tot8 = akh;                         // f32 [8][128] 8-row group sums   } P1/P2
-    static constexpr int first = akh + 8 * KD * 4;           // f32 [128] G of row 0              } only
+    static constexpr int tot = bk;                           // f32 [4][128] 16-row group sums } P1/P2
+    static constexpr int first = bk + 4 * KD * 4;            // f32 [128] G of row 0           } only
     static constexpr int total = dt + VT * C * 2;
 };
+// mbarriers: chunk loads, A MMA, S1 MMA, S3 MMA, operands ready, slot 0 / 1 released
+struct Bar { enum { load = 0, a = 1, s1 = 2, s3 = 3, ready = 4, free0 = 5 }; };
 static_assert(Smem::total <= 232448, "shared memory budget");
 static_assert(Smem::aop % 1024 == 0 && Smem::bk % 1024 == 0 && Smem::kht % 1024 == 0 &&
-              Smem::akh % 1024 == 0 && Smem::aqk % 1024 == 0 && Smem::ht % 1024 == 0 &&
-              Smem::dt % 1024 == 0, "SW128 tiles need 1024-byte alignment");
-static_assert(Smem::first + KD * 4 <= Smem::ht, "gate group sums fit in the A_kk / A_qk space");
+              Smem::akh % 1024 == 0 && Smem::ht % 1024 == 0 && Smem::dt % 1024 == 0,
+              "SW128 tiles need 1024-byte alignment");
+static_assert(VT * LD64 * 2 <= VT * KD * 2, "(beta X)^T fits in the h^T space");
+static_assert(Smem::first + KD * 4 <= Smem::kht, "gate group sums fit in the b space");
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -205,9 +212,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int count)
 {
     asm volatile("bar.sync %0, %1;\n" :: "r"(id), "r"(count) : "memory");
 }
-__device__ __forceinline__ void named_bar_arrive(int id, int count)
+// named barrier over `count` threads that also ORs `pred` across them
+__device__ __forceinline__ bool bar_red_or(int id, int count, bool pred)
 {
-    asm volatile("bar.arrive %0, %1;\n" :: "r"(id), "r"(count) : "memory");
+    int r;
+    asm volatile("{\n.reg .pred p, q;\nsetp.ne.b32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\n"
+                 "selp.b32 %0, 1, 0, q;\n}\n"
+                 : "=r"(r) : "r"((int)pred), "r"(id), "r"(count) : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" :: "r"(mbar) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -345,7 +362,7 @@ __device__ __forceinline__ void issue_chunk_loads(unsigned char *sm, const Prefi
     }
     cp_async_commit();
     if (lane == 0) {
-        const uint32_t mbar = smem_u32(sm + Smem::mbar);
+        const uint32_t mbar = smem_u32(sm + Smem::bars + 8 * Bar::load);
         fence_proxy_async_smem();   // earlier generic reads of the raw buffers come first
         const uint32_t bytes = C * (2 * KD * 2 + KD * 4 + VT * 2) + (maps.beta_tma ? C * 16 : 0);
         mbar_arrive_expect_tx(mbar, bytes);
@@ -358,10 +375,10 @@ __device__ __forceinline__ void issue_chunk_loads(unsigned char *sm, const Prefi
     }
 }
 
-// Zero the rows [len, 64) of the raw tiles (tokens of the next sequence).
-__device__ __forceinline__ void zero_tail_rows(unsigned char *sm, int len, int tid)
+// Zero the rows [len, 64) of the raw tiles (tokens of the next sequence); one group.
+__device__ __forceinline__ void zero_tail_rows(unsigned char *sm, int len, int gtid)
 {
-    for (int e = tid; e < (C - len) * KD / 8; e += kThreads) {   // 16 B per store
+    for (int e = gtid; e < (C - len) * KD / 8; e += kGroup) {   // 16 B per store
         const int r = len + e / (KD / 8), piece = e % (KD / 8);
         const uint4 z = make_uint4(0, 0, 0, 0);
         *reinterpret_cast<uint4 *>(sm + Smem::q_raw + (r * KD + piece * 8) * 2) = z;
@@ -395,25 +412,23 @@ __device__ __forceinline__ void store_row16(__nv_bfloat16 *dst, const float (&v)
 }
 
 // Exact-exponential intra-chunk matrices for chunks whose gate span leaves the fp16
-// fast path.  Recomputes the exp2-space cumsum G in place in g_raw, then writes A_kk
+// fast path (run by the operand group).  Recomputes the exp2-space cumsum G in place
+// in g_raw, then writes A_kk
 // and A_qk (fp16, zeros above the diagonal) with one exponential per pair and
 // channel, and K^^T with one exponential per element (its fast-path values can
 // overflow at such spans).
-__device__ __noinline__ void exact_intra_chunk(unsigned char *sm, int tid)
+__device__ __noinline__ void exact_intra_chunk(unsigned char *sm, int gtid, const float *beta,
+                                               __half *akh, __half *aqk, __half *kht)
 {
     const __nv_bfloat16 *qr = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::q_raw);
     const __nv_bfloat16 *kr = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::k_raw);
     float *G = reinterpret_cast<float *>(sm + Smem::g_raw);
-    const float *beta = reinterpret_cast<const float *>(sm + Smem::beta);
-    __half *akh = reinterpret_cast<__half *>(sm + Smem::akh);
-    __half *aqk = reinterpret_cast<__half *>(sm + Smem::aqk);
-    __half *kht = reinterpret_cast<__half *>(sm + Smem::kht);
-    if (tid < KD) {
+    if (gtid < KD) {
         float acc = 0.f;
-        for (int r = 0; r < C; ++r) { acc += G[r * KD + tid] * kLog2e; G[r * KD + tid] = acc; }
+        for (int r = 0; r < C; ++r) { acc += G[r * KD + gtid] * kLog2e; G[r * KD + gtid] = acc; }
     }
-    __syncthreads();
-    for (int p = tid; p < C * (C + 1) / 2; p += kThreads) {
+    named_bar_sync(kBarPrep, kGroup);
+    for (int p = gtid; p < C * (C + 1) / 2; p += kGroup) {
         int r = (int)((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
         while (r * (r + 1) / 2 > p) --r;
         while ((r + 1) * (r + 2) / 2 <= p) ++r;
@@ -431,7 +446,7 @@ __device__ __noinline__ void exact_intra_chunk(unsigned char *sm, int tid)
             aqk[sw128(i, r, C)] = __float2half_rn(0.f);
         }
     }
-    for (int e = tid; e < C * KD; e += kThreads) {
+    for (int e = gtid; e < C * KD; e += kGroup) {
         const int r = e >> 7, c = e & 127;
         const float gr = G[r * KD + c], gl = G[(C - 1) * KD + c];
         kht[sw128(c, r, KD)] = __float2half_rn(__bfloat162float(kr[r * KD + c]) * exp2f(gl - gr));
@@ -439,39 +454,89 @@ __device__ __noinline__ void exact_intra_chunk(unsigned char *sm, int tid)
 }
 
 // T_RR = (I + A_RR)^-1 of the 16x16 diagonal blocks R = 2 P and 2 P + 1 by fp32
-// forward substitution on the fp16 A_kk: half-warp R % 2, lane j owns column j of
-// block R; row rr + 1 of the block is loaded (two 16-byte pieces, a broadcast read)
-// while row rr is reduced.  Written to T (fp16) with its zeros and unit diagonal.
-__device__ __forceinline__ void invert_diag_blocks(const __half *akh, __half *tmh, int P, int lane)
+// forward substitution on the fp16 A_kk, right-looking: half-warp R % 2, lane j owns
+// column j of block R; once T[m][j] is final, every row below it is updated,
+//     T[r][j] -= A[r][m] T[m][j]    (r > m),
+// so the dependent chain is one multiply-add per step.  Columns m, m + 1 of A are
+// read as one 4-byte broadcast per row.  Written to tdg[R][16][16] (fp16) with its
+// zeros and unit diagonal.
+__device__ __forceinline__ void invert_diag_blocks(const __half *akh, __half *tdg, int P, int lane)
 {
     const int j = lane & 15, R = 2 * P + (lane >> 4);
     float col[16];
 #pragma unroll
     for (int m = 0; m < 16; ++m) col[m] = (m == j) ? 1.f : 0.f;
-    auto piece = [&](int rr, int hf) {
-        const int row = 16 * R + rr;
-        return *reinterpret_cast<const uint4 *>(akh + row * C + (((2 * R + hf) ^ (row & 7)) << 3));
-    };
-    uint4 n0 = piece(1, 0), n1 = piece(1, 1);
 #pragma unroll
-    for (int rr = 1; rr < 16; ++rr) {
-        const uint4 c0 = n0, c1 = n1;
-        if (rr < 15) { n0 = piece(rr + 1, 0); n1 = piece(rr + 1, 1); }
-        float av[16];
-        const __half2 *p0 = reinterpret_cast<const __half2 *>(&c0);
-        const __half2 *p1 = reinterpret_cast<const __half2 *>(&c1);
+    for (int mp = 0; mp < 8; ++mp) {
+        const int m = 2 * mp;
+        float2 am[16];   // (A[r][m], A[r][m + 1]) for r > m
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float2 x0 = __half22float2(p0[u]), x1 = __half22float2(p1[u]);
-            av[2 * u] = x0.x; av[2 * u + 1] = x0.y; av[8 + 2 * u] = x1.x; av[8 + 2 * u + 1] = x1.y;
-        }
-        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = m + 1; r < 16; ++r)
+            am[r] = __half22float2(*reinterpret_cast<const __half2 *>(akh + sw128(16 * R + r, 16 * R + m, C)));
 #pragma unroll
-        for (int m = 0; m < rr; ++m) s4[m & 3] += av[m] * col[m];
-        if (j < rr) col[rr] = -((s4[0] + s4[1]) + (s4[2] + s4[3]));
+        for (int r = m + 1; r < 16; ++r) col[r] -= am[r].x * col[m];
+#pragma unroll
+        for (int r = m + 2; r < 16; ++r) col[r] -= am[r].y * col[m + 1];
     }
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) tmh[(16 * R + rr) * LD64 + 16 * R + j] = __float2half_rn(col[rr]);
+    for (int rr = 0; rr < 16; ++rr) tdg[(16 * R + rr) * 16 + j] = __float2half_rn(col[rr]);
+}
+
+// T_RI (R > I) of column block I, top to bottom, by ONE warp (no barrier between the
+// blocks of a column: each needs only T_JI, I <= J < R, of the same column):
+//     T_RI = -T_RR sum_{J=I}^{R-1} A_RJ T_JI
+// on tensor cores, evaluated transposed (X^T = sum T_JI^T A_RJ^T, then
+// T_RI^T = -X^T T_RR^T) so X^T passes from accumulator to operand in registers.
+__device__ __forceinline__ void solve_column_block(const __half *akh, __half *tmh, int I, int lane)
+{
+    const int g8 = lane >> 2, tig = lane & 3;
+#pragma unroll
+    for (int R = I + 1; R < 4; ++R) {
+        float xj[3][2][4];   // one accumulator per J, summed afterwards (no chained mma)
+#pragma unroll
+        for (int J = I; J < R; ++J) {
+            float (&xa)[2][4] = xj[J - I];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) xa[t][0] = xa[t][1] = xa[t][2] = xa[t][3] = 0.f;
+            uint32_t af[4], bf[4];
+            // A = T_JI^T (rows i, cols m) from T_JI stored [m][i]
+            ldsm_x4_t(smem_u32(tmh + (16 * J + (lane & 7) + ((lane >> 4) << 3)) * LD64 +
+                               16 * I + (((lane >> 3) & 1) << 3)),
+                      af[0], af[1], af[2], af[3]);
+            // B = A_RJ^T as [k=m][n=r] from A_RJ stored (swizzled) [r][m]
+            const int bn = 16 * R + (lane & 7) + ((lane >> 4) << 3);
+            const int bkk = 16 * J + (((lane >> 3) & 1) << 3);
+            ldsm_x4(smem_u32(akh + sw128(bn, bkk, C)), bf[0], bf[1], bf[2], bf[3]);
+            mma16816(xa[0], af, bf[0], bf[1]);
+            mma16816(xa[1], af, bf[2], bf[3]);
+        }
+        float xa[2][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float acc = xj[0][t][e];
+#pragma unroll
+                for (int J = I + 1; J < R; ++J) acc += xj[J - I][t][e];
+                xa[t][e] = acc;
+            }
+        const uint32_t xf[4] = {pack_h2(-xa[0][0], -xa[0][1]), pack_h2(-xa[0][2], -xa[0][3]),
+                                pack_h2(-xa[1][0], -xa[1][1]), pack_h2(-xa[1][2], -xa[1][3])};
+        uint32_t tb[4];
+        ldsm_x4(smem_u32(tmh + bnk_off(lane, 16 * R, 16 * R, LD64)), tb[0], tb[1], tb[2], tb[3]);
+        float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        mma16816(ta[0], xf, tb[0], tb[1]);
+        mma16816(ta[1], xf, tb[2], tb[3]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = 16 * I + g8 + ((e >> 1) << 3);
+                const int rr = 16 * R + 8 * nt + 2 * tig + (e & 1);
+                tmh[rr * LD64 + i] = __float2half_rn(ta[nt][e]);
+            }
+        __syncwarp();   // T_RI is read (ldmatrix, other lanes) by the next block of the column
+    }
 }
 
 template <typename Tout>
@@ -486,26 +551,19 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     const int h = blockIdx.y;
     const int H = a.num_heads;
 
-    const float *graw = reinterpret_cast<const float *>(sm + Smem::g_raw);
-    const __nv_bfloat16 *qraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::q_raw);
-    const __nv_bfloat16 *kraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::k_raw);
-    const float *braw = reinterpret_cast<const float *>(sm + Smem::b_raw);
-    __half *tmh = reinterpret_cast<__half *>(sm + Smem::tm);
     __half *aop = reinterpret_cast<__half *>(sm + Smem::aop);
-    __half *bop = reinterpret_cast<__half *>(sm + Smem::bk);
-    __half *kht = reinterpret_cast<__half *>(sm + Smem::kht);
-    __half *akh = reinterpret_cast<__half *>(sm + Smem::akh);
-    __half *aqk = reinterpret_cast<__half *>(sm + Smem::aqk);
     __half *ht = reinterpret_cast<__half *>(sm + Smem::ht);
     __half *dt = reinterpret_cast<__half *>(sm + Smem::dt);
     __half *xt = reinterpret_cast<__half *>(sm + Smem::xt);
-    __nv_bfloat16 *vs = reinterpret_cast<__nv_bfloat16 *>(sm + Smem::vs);
-    float *beta_s = reinterpret_cast<float *>(sm + Smem::beta);
-    float *dec = reinterpret_cast<float *>(sm + Smem::dec);
-    float *pm = reinterpret_cast<float *>(sm + Smem::pm);
-    float *tot8 = reinterpret_cast<float *>(sm + Smem::tot8);
-    float *first = reinterpret_cast<float *>(sm + Smem::first);
-    volatile int *flag = reinterpret_cast<volatile int *>(sm + Smem::flag);
+    // slot buffers of chunk parity s
+    auto vs_s = [&](int s) { return reinterpret_cast<__nv_bfloat16 *>(sm + Smem::vs) + s * C * VT; };
+    auto beta_s = [&](int s) { return reinterpret_cast<float *>(sm + Smem::beta) + s * C; };
+    auto dec_s = [&](int s) { return reinterpret_cast<float *>(sm + Smem::dec) + s * KD; };
+    auto pm_s = [&](int s) { return reinterpret_cast<float *>(sm + Smem::pm) + s * KD; };
+    auto tdg_s = [&](int s) { return reinterpret_cast<__half *>(sm + Smem::tdg) + s * 4 * 16 * 16; };
+    auto kht_s = [&](int s) { return reinterpret_cast<__half *>(sm + Smem::kht) + s * KD * C; };
+    auto akh_s = [&](int s) { return reinterpret_cast<__half *>(sm + Smem::akh) + s * 2 * C * C; };
+    auto bar = [&](int b) { return smem_u32(sm + Smem::bars + 8 * b); };
 
     int64_t bos, eos;
     clamp_range(a.total_tokens, a.cu_seqlens[n], a.cu_seqlens[n + 1], bos, eos);
@@ -515,88 +573,78 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
 
     // ---- tensor memory (128 columns: [0, 32) the step accumulator D1, [32, 64) the
     //      state h^T with lane = key channel, column = value, [64, 128) the A matrices)
-    //      and the three mbarriers
-    const uint32_t mbar = smem_u32(sm + Smem::mbar);
-    const uint32_t mbar_a = smem_u32(sm + Smem::mbar_a);
-    const uint32_t mbar_mma = smem_u32(sm + Smem::mbar_mma);
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
                      :: "r"(smem_u32(sm + Smem::tmem)), "r"(128) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
-    if (tid == 0) {
-        mbar_init(mbar, 1);
-        mbar_init(mbar_a, 1);
-        mbar_init(mbar_mma, 1);
-    }
+    if (tid == 0)
+        for (int b = 0; b <= Bar::free0 + 1; ++b) mbar_init(bar(b), 1);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Smem::tmem);
     const uint32_t tD1 = tmem, tH = tmem + 32, tDA = tmem + 64;
-
-    // TMEM roles (warp w reaches lanes 32 (w % 4) .. +31):
-    //   state warps 8..15: key channels sc = 32 (w % 4) + lane, value columns [16 hc, 16 hc + 16)
-    //   A matrices (lanes 0..63 A_kk, 64..127 A_qk): warps 0..7, columns [32 (w / 4), +32)
-    //   X rows (lanes 0..63): warps 0, 1 (columns 0..15) and 4, 5 (columns 16..31)
-    //   o rows (lanes 64..127): warps 2, 3 (columns 0..15) and 6, 7 (columns 16..31)
-    const bool state_warp = warp >= 8;
-    const int sc = 32 * (warp & 3) + lane;                       // key channel of a state warp
-    const int hc = (warp >> 2) & 1;                              // its half of the value columns
-    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;  // TMEM lane quadrant
-    if (state_warp) {   // initial state -> tensor memory
-        float hv[16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float4 x = init ? *reinterpret_cast<const float4 *>(init + (int64_t)sc * VD + vt * VT + 16 * hc + 4 * j)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-            hv[4 * j] = x.x; hv[4 * j + 1] = x.y; hv[4 * j + 2] = x.z; hv[4 * j + 3] = x.w;
-        }
-        tmem_st16(tH + lane_off + 16 * hc, hv);
-        tc_fence_before();
-    }
-
-    constexpr int kLoadWarp = kThreads / 32 - 1;   // issues every chunk's loads
-    if (bos < eos && warp == kLoadWarp)
-        issue_chunk_loads(sm, a, maps, bos, (int)((eos - bos) < C ? (eos - bos) : C), h, vt, lane);
-
-    Tout *out = static_cast<Tout *>(a.out);
-    uint32_t load_parity = 0, a_parity = 0, mma_parity = 0;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;   // TMEM lane quadrant of this warp
     bool failed = false;
 
-    for (int64_t t0 = bos; t0 < eos; t0 += C) {
-        const int len = (int)((eos - t0) < C ? (eos - t0) : C);
-        cp_async_wait_all();
-        if (!mbar_wait(mbar, load_parity)) failed = true;   // loads did not land: stop
-        load_parity ^= 1u;
-        if (!failed && len < C) zero_tail_rows(sm, len, tid);
-        if (__syncthreads_or(failed)) { failed = true; break; }
-        tc_fence_after();
-        if (tid == 0) *flag = 0;
+    if (warp >= 8) {
+        // =====================================================================
+        // Operand group (warps 8..15): for chunk n, the gate cumsum, reference and
+        // factors, the fp16 operands and A_kk / A_qk (tcgen05 + epilogue), into
+        // slot n % 2; it runs one chunk ahead of the state-step group.
+        // =====================================================================
+        const int gtid = tid - kGroup;
+        constexpr int kLoadWarp = 15;   // issues every chunk's loads
+        if (bos < eos && warp == kLoadWarp)
+            issue_chunk_loads(sm, a, maps, bos, (int)((eos - bos) < C ? (eos - bos) : C), h, vt, lane);
+        const float *graw = reinterpret_cast<const float *>(sm + Smem::g_raw);
+        const __nv_bfloat16 *qraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::q_raw);
+        const __nv_bfloat16 *kraw = reinterpret_cast<const __nv_bfloat16 *>(sm + Smem::k_raw);
+        const float *braw = reinterpret_cast<const float *>(sm + Smem::b_raw);
+        __half *bop = reinterpret_cast<__half *>(sm + Smem::bk);
+        float *tot = reinterpret_cast<float *>(sm + Smem::tot);
+        float *first = reinterpret_cast<float *>(sm + Smem::first);
+        volatile int *flag = reinterpret_cast<volatile int *>(sm + Smem::flag);
+        uint32_t load_parity = 0, a_parity = 0;
 
-        // ---------------- P1: in-chunk gate cumsum, exp2 space; thread = (channel pair, 8-row group E)
-        const int pcp = tid & 63, pE = tid >> 6, pc0 = 2 * pcp;
-        float2 gx[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const float2 g2 = *reinterpret_cast<const float2 *>(graw + (8 * pE + u) * KD + pc0);
-            gx[u] = make_float2(g2.x * kLog2e, g2.y * kLog2e);
-        }
-#pragma unroll
-        for (int u = 1; u < 8; ++u) { gx[u].x += gx[u - 1].x; gx[u].y += gx[u - 1].y; }
-        *reinterpret_cast<float2 *>(tot8 + pE * KD + pc0) = gx[7];
-        if (pE == 0) *reinterpret_cast<float2 *>(first + pc0) = gx[0];
-        if (tid < C * VT * 2 / 16)   // copy v (4 KB) out of the raw buffer, 16 B per thread
-            reinterpret_cast<uint4 *>(vs)[tid] = reinterpret_cast<const uint4 *>(sm + Smem::v_raw)[tid];
-        if (tid < C) beta_s[tid] = tid < len ? braw[tid * 4 + (maps.beta_tma ? (h & 3) : 0)] : 0.f;
-        __syncthreads();
+        int ci = 0;
+        for (int64_t t0 = bos; t0 < eos; t0 += C, ++ci) {
+            const int len = (int)((eos - t0) < C ? (eos - t0) : C);
+            const int s = ci & 1;
+            __half *kht = kht_s(s), *akh = akh_s(s), *aqk = akh + C * C;
+            float *bs = beta_s(s);
+            // slot s is free once the step of chunk ci - 2 has ended
+            if (ci >= 2 && !mbar_wait(bar(Bar::free0 + s), ((ci - 2) >> 1) & 1)) failed = true;
+            cp_async_wait_all();
+            if (!mbar_wait(bar(Bar::load), load_parity)) failed = true;   // loads did not land: stop
+            load_parity ^= 1u;
+            if (!failed && len < C) zero_tail_rows(sm, len, gtid);
+            if (bar_red_or(kBarPrep, kGroup, failed)) { failed = true; break; }
+            if (gtid == 0) *flag = 0;
 
-        // ---------------- P2: reference, factors and the fp16 tcgen05 operands
-        {
+            // ---------------- P1: in-chunk gate cumsum, exp2 space; thread = (channel pair, 16-row group E)
+            const int pcp = gtid & 63, pE = gtid >> 6, pc0 = 2 * pcp;
+            float2 gx[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const float2 g2 = *reinterpret_cast<const float2 *>(graw + (16 * pE + u) * KD + pc0);
+                gx[u] = make_float2(g2.x * kLog2e, g2.y * kLog2e);
+            }
+#pragma unroll
+            for (int u = 1; u < 16; ++u) { gx[u].x += gx[u - 1].x; gx[u].y += gx[u - 1].y; }
+            *reinterpret_cast<float2 *>(tot + pE * KD + pc0) = gx[15];
+            if (pE == 0) *reinterpret_cast<float2 *>(first + pc0) = gx[0];
+            // v (4 KB) and beta of this chunk into slot s
+            reinterpret_cast<uint4 *>(vs_s(s))[gtid] = reinterpret_cast<const uint4 *>(sm + Smem::v_raw)[gtid];
+            if (gtid < C) bs[gtid] = gtid < len ? braw[gtid * 4 + (maps.beta_tma ? (h & 3) : 0)] : 0.f;
+            named_bar_sync(kBarPrep, kGroup);
+
+            // ---------------- P2: reference, factors and the fp16 tcgen05 operands
             float2 pre = make_float2(0.f, 0.f), run = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int E = 0; E < 8; ++E) {
-                const float2 t = *reinterpret_cast<const float2 *>(tot8 + E * KD + pc0);
+            for (int E = 0; E < 4; ++E) {
+                const float2 t = *reinterpret_cast<const float2 *>(tot + E * KD + pc0);
                 if (E == pE) pre = run;
                 run.x += t.x; run.y += t.y;
             }
@@ -606,99 +654,76 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
             const float mx_ = fmaxf(0.5f * (g0.x + glast.x), g0.x - 0.5f * kSpanMax);
             const float my_ = fmaxf(0.5f * (g0.y + glast.y), g0.y - 0.5f * kSpanMax);
             if (pE == 0) {
-                *reinterpret_cast<float2 *>(pm + pc0) = make_float2(exp2f(mx_), exp2f(my_));
-                *reinterpret_cast<float2 *>(dec + pc0) = make_float2(exp2f(glast.x), exp2f(glast.y));
+                *reinterpret_cast<float2 *>(pm_s(s) + pc0) = make_float2(exp2f(mx_), exp2f(my_));
+                *reinterpret_cast<float2 *>(dec_s(s) + pc0) = make_float2(exp2f(glast.x), exp2f(glast.y));
             }
             const float fx = exp2f(glast.x - mx_), fy = exp2f(glast.y - my_);   // K^ = b 2^(G_last - m)
             const float bx = pre.x - mx_, by = pre.y - my_;                    // G_r - m = gx + b
-            float khx[8], khy[8], amax = 0.f;
+            named_bar_sync(kBarPrep, kGroup);   // the group sums (in the b space) are read
+            // [a_k; a_q] of the previous chunk is read by its S1 MMA: wait for it
+            if (ci >= 1 && !mbar_wait(bar(Bar::s1), (ci - 1) & 1)) failed = true;
+            float amax = 0.f;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int r = 8 * pE + u;
-                const float xx = gx[u].x + bx, xy = gx[u].y + by;   // G_r - m
-                amax = fmaxf(amax, fmaxf(fabsf(xx), fabsf(xy)));
-                const float ex = exp2f(xx), ey = exp2f(xy);
-                const float ix = rcp_approx(ex), iy = rcp_approx(ey);
-                const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(kraw + r * KD + pc0));
-                const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qraw + r * KD + pc0));
-                *reinterpret_cast<uint32_t *>(aop + sw128(r, pc0, 2 * C)) = pack_h2(kv.x * ex, kv.y * ey);
-                *reinterpret_cast<uint32_t *>(aop + sw128(C + r, pc0, 2 * C)) = pack_h2(qv.x * ex, qv.y * ey);
-                const float b0 = kv.x * ix, b1 = kv.y * iy;
-                *reinterpret_cast<uint32_t *>(bop + sw128(r, pc0, C)) = pack_h2(b0, b1);
-                khx[u] = b0 * fx;
-                khy[u] = b1 * fy;
+            for (int hb = 0; hb < 2; ++hb) {
+                float khx[8], khy[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int r = 16 * pE + 8 * hb + u;
+                    const float xx = gx[8 * hb + u].x + bx, xy = gx[8 * hb + u].y + by;   // G_r - m
+                    amax = fmaxf(amax, fmaxf(fabsf(xx), fabsf(xy)));
+                    const float ex = exp2f(xx), ey = exp2f(xy);
+                    const float ix = rcp_approx(ex), iy = rcp_approx(ey);
+                    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(kraw + r * KD + pc0));
+                    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(qraw + r * KD + pc0));
+                    *reinterpret_cast<uint32_t *>(aop + sw128(r, pc0, 2 * C)) = pack_h2(kv.x * ex, kv.y * ey);
+                    *reinterpret_cast<uint32_t *>(aop + sw128(C + r, pc0, 2 * C)) = pack_h2(qv.x * ex, qv.y * ey);
+                    const float b0 = kv.x * ix, b1 = kv.y * iy;
+                    *reinterpret_cast<uint32_t *>(bop + sw128(r, pc0, C)) = pack_h2(b0, b1);
+                    khx[u] = b0 * fx;
+                    khy[u] = b1 * fy;
+                }
+                // K^^T: these eight rows are one 16-byte chunk of key-channel row c
+                const int r0 = 16 * pE + 8 * hb;
+                *reinterpret_cast<uint4 *>(kht + sw128(pc0, r0, KD)) =
+                    make_uint4(pack_h2(khx[0], khx[1]), pack_h2(khx[2], khx[3]),
+                               pack_h2(khx[4], khx[5]), pack_h2(khx[6], khx[7]));
+                *reinterpret_cast<uint4 *>(kht + sw128(pc0 + 1, r0, KD)) =
+                    make_uint4(pack_h2(khy[0], khy[1]), pack_h2(khy[2], khy[3]),
+                               pack_h2(khy[4], khy[5]), pack_h2(khy[6], khy[7]));
             }
-            // K^^T: the eight rows of this group are one 16-byte chunk of key-channel row c
-            *reinterpret_cast<uint4 *>(kht + sw128(pc0, 8 * pE, KD)) =
-                make_uint4(pack_h2(khx[0], khx[1]), pack_h2(khx[2], khx[3]),
-                           pack_h2(khx[4], khx[5]), pack_h2(khx[6], khx[7]));
-            *reinterpret_cast<uint4 *>(kht + sw128(pc0 + 1, 8 * pE, KD)) =
-                make_uint4(pack_h2(khy[0], khy[1]), pack_h2(khy[2], khy[3]),
-                           pack_h2(khy[4], khy[5]), pack_h2(khy[6], khy[7]));
             // fast path: every factor 2^(G_r - m) within [2^-8, 2^8]
             if (__any_sync(0xffffffffu, !(amax <= 0.5f * kSpanMax)) && lane == 0) *flag = 1;
-            fence_proxy_async_smem();   // the operands are read by tcgen05 below
-        }
-        __syncthreads();
-        const bool exact_path = *flag != 0;
+            fence_proxy_async_smem();   // the operands are read by tcgen05
+            named_bar_sync(kBarPrep, kGroup);
+            const bool exact_path = *flag != 0;
 
-        // ---------------- MMA A: [A_kk'; A_qk'] = [a_k; a_q] b^T  (fast path)
-        if (!exact_path && tid == 0) {
-            tc_fence_after();
+            if (!exact_path) {
+                // ---------------- MMA A: [A_kk'; A_qk'] = [a_k; a_q] b^T
+                if (gtid == 0) {
+                    tc_fence_after();
 #pragma unroll
-            for (int ks = 0; ks < KD / 16; ++ks)
-                umma_f16(tDA, sw128_kdesc(smem_u32(aop), ks, 2 * C), sw128_kdesc(smem_u32(bop), ks, C),
-                         kIdescM128N64, ks > 0);
-            umma_commit(mbar_a);
-        }
-        // The raw buffers are free once P2 has read them, except on the exact path,
-        // which reads them below: the load warp fetches the next chunk now (or, on the
-        // exact path, after the intra-chunk matrices) so the copies overlap the rest.
-        if (warp == kLoadWarp && !exact_path && t0 + C < eos) {
-            const int64_t t1 = t0 + C;
-            issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, lane);
-        }
-        // ---------------- state warps: fp16 copy (2^m h)^T for S1, then h <- Diag(2^G_last) h
-        constexpr int kS1Bar = 6, kS1Threads = 9 * 32;   // state warps + warp 0
-        if (state_warp) {
-            tc_fence_after();
-            float hv[16];
-            tmem_ld16(tH + lane_off + 16 * hc, hv);
-            const float p = pm[sc], d = dec[sc];
-#pragma unroll
-            for (int v = 0; v < 16; ++v) {
-                ht[sw128(16 * hc + v, sc, VT)] = __float2half_rn(p * hv[v]);
-                hv[v] *= d;
-            }
-            tmem_st16(tH + lane_off + 16 * hc, hv);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            named_bar_arrive(kS1Bar, kS1Threads);
-        } else if (warp == 0) {
-            named_bar_sync(kS1Bar, kS1Threads);
-            // ---------------- MMA S1: D1 = [a_k; a_q] (2^m h) = [K~ h; Q~ h]
-            if (tid == 0) {
+                    for (int ks = 0; ks < KD / 16; ++ks)
+                        umma_f16(tDA, sw128_kdesc(smem_u32(aop), ks, 2 * C), sw128_kdesc(smem_u32(bop), ks, C),
+                                 kIdescM128N64, ks > 0);
+                    umma_commit(bar(Bar::a));
+                }
+                // the raw buffers are free: fetch the next chunk
+                if (warp == kLoadWarp && t0 + C < eos) {
+                    const int64_t t1 = t0 + C;
+                    issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, lane);
+                }
+                // ---------------- A epilogue: masked, beta-scaled fp16 A_kk and A_qk
+                //   lanes 0..63 A_kk, 64..127 A_qk; warp w: lane quadrant w % 4, columns [32 ((w / 4) % 2), +32)
+                if (!mbar_wait(bar(Bar::a), a_parity)) failed = true;
+                a_parity ^= 1u;
                 tc_fence_after();
-#pragma unroll
-                for (int ks = 0; ks < KD / 16; ++ks)
-                    umma_f16(tD1, sw128_kdesc(smem_u32(aop), ks, 2 * C), sw128_kdesc(smem_u32(ht), ks, VT),
-                             kIdescM128N32, ks > 0);
-                umma_commit(mbar_mma);
-            }
-        }
-
-        // ---------------- A epilogue: masked, beta-scaled fp16 A_kk and A_qk
-        if (!exact_path) {
-            if (warp < 8) {
-                if (!mbar_wait(mbar_a, a_parity)) failed = true;
-                tc_fence_after();
-                const int c0 = 32 * (warp >> 2), rg = 32 * (warp & 3) + lane;
+                const int c0 = 32 * ((warp >> 2) & 1), rg = 32 * (warp & 3) + lane;
                 float av[2][16];
-                tmem_ld16(tDA + ((uint32_t)(32 * (warp & 3)) << 16) + c0, av[0]);
-                tmem_ld16(tDA + ((uint32_t)(32 * (warp & 3)) << 16) + c0 + 16, av[1]);
+                tmem_ld16(tDA + lane_off + c0, av[0]);
+                tmem_ld16(tDA + lane_off + c0 + 16, av[1]);
                 const bool kk = rg < C;
                 const int r = kk ? rg : rg - C;
-                const float sb = kk ? beta_s[r] : 1.f;
+                const float sb = kk ? bs[r] : 1.f;
                 const int lim = kk ? r : r + 1;   // columns i < lim are kept
                 __half *dst = kk ? akh : aqk;
 #pragma unroll
@@ -714,148 +739,197 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
                     *reinterpret_cast<uint4 *>(dst + sw128(r, c0 + 8 * t, C)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 tc_fence_before();
-            }
-            a_parity ^= 1u;
-        } else {
-            exact_intra_chunk(sm, tid);
-        }
-        fence_proxy_async_smem();   // A_qk, A_kk and K^^T are read by tcgen05 below
-        __syncthreads();
-        if (warp == kLoadWarp && exact_path && t0 + C < eos) {
-            const int64_t t1 = t0 + C;
-            issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, lane);
-        }
-
-        // ---------------- diagonal blocks of T (warps 10, 11) || X = beta (v - K~ h) (warps 0, 1, 4, 5)
-        if (warp == 10 || warp == 11) invert_diag_blocks(akh, tmh, warp - 10, lane);
-        if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {   // rows 0..63 of D1: K~ h
-            if (!mbar_wait(mbar_mma, mma_parity)) failed = true;
-            tc_fence_after();
-            const int r = 32 * (warp & 1) + lane, half = warp >> 2;
-            float xv[16];
-            tmem_ld16(tD1 + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, xv);
-            const float b = beta_s[r];
-            const uint4 *vrow = reinterpret_cast<const uint4 *>(vs + r * VT + 16 * half);
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const uint4 w = vrow[j];
-                const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&w);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 vv = __bfloat1622float2(p2[u]);
-                    const int v = 8 * j + 2 * u;
-                    xt[(16 * half + v) * LD64 + r] = __float2half_rn(b * (vv.x - xv[v]));
-                    xt[(16 * half + v + 1) * LD64 + r] = __float2half_rn(b * (vv.y - xv[v + 1]));
+                // diagonal blocks of T: warp 8 stored A_kk rows 0..31 x columns 0..31 (blocks 0, 1),
+                // warp 13 rows 32..63 x columns 32..63 (blocks 2, 3)
+                if (warp == 8 || warp == 13) {
+                    __syncwarp();
+                    invert_diag_blocks(akh, tdg_s(s), warp == 13, lane);
+                }
+            } else {
+                exact_intra_chunk(sm, gtid, bs, akh, aqk, kht);
+                named_bar_sync(kBarPrep, kGroup);
+                if (warp == 8 || warp == 13) invert_diag_blocks(akh, tdg_s(s), warp == 13, lane);
+                if (warp == kLoadWarp && t0 + C < eos) {
+                    const int64_t t1 = t0 + C;
+                    issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, lane);
                 }
             }
+            fence_proxy_async_smem();   // A_kk, A_qk and K^^T are read by tcgen05 in the state step
+            named_bar_sync(kBarPrep, kGroup);
+
+            // operands of chunk ci are complete: hand slot s to the state step
+            if (bar_red_or(kBarPrep, kGroup, failed)) { failed = true; break; }
+            if (gtid == 0) mbar_arrive(bar(Bar::ready));
+        }
+        if (failed) {   // copies or MMAs still in flight get one more bounded wait
+            mbar_wait(bar(Bar::load), load_parity);
+            mbar_wait(bar(Bar::a), a_parity);
+        }
+    } else {
+        // =====================================================================
+        // State-step group (warps 0..7): per chunk, once its operands are ready,
+        //   the scaled fp16 copy of h and the decay of h, S1, then T = (I + A_kk)^-1
+        //   (warps 2, 3, 6) while warps 0, 1, 4, 5 form X = beta (v - K~ h), then
+        //   D = T X, S3 and the output.  Warp w reaches TMEM lanes 32 (w % 4) ..;
+        //   state roles: key channel sc = 32 (w % 4) + lane, value columns [16 hc, +16).
+        // =====================================================================
+        const int sc = 32 * (warp & 3) + lane;
+        const int hc = (warp >> 2) & 1;
+        {   // initial state -> tensor memory
+            float hv[16];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 x = init ? *reinterpret_cast<const float4 *>(init + (int64_t)sc * VD + vt * VT + 16 * hc + 4 * j)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                hv[4 * j] = x.x; hv[4 * j + 1] = x.y; hv[4 * j + 2] = x.z; hv[4 * j + 3] = x.w;
+            }
+            tmem_st16(tH + lane_off + 16 * hc, hv);
             tc_fence_before();
         }
-        mma_parity ^= 1u;
-        __syncthreads();
-
-        // ---------------- T below the diagonal blocks, by distance from the diagonal:
-        //     T_RI = -T_RR sum_{J=I}^{R-1} A_RJ T_JI
-        // on tensor cores, evaluated transposed (X^T = sum T_JI^T A_RJ^T, then
-        // T_RI^T = -X^T T_RR^T) so X^T passes from accumulator to operand in registers.
-#pragma unroll 1
-        for (int lvl = 1; lvl < 4; ++lvl) {
-            if (warp < 4 - lvl) {
-                const int I = warp, R = warp + lvl;
-                float xa[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                for (int J = I; J < R; ++J) {
-                    uint32_t af[4], bf[4];
-                    // A = T_JI^T (rows i, cols m) from T_JI stored [m][i]
-                    ldsm_x4_t(smem_u32(tmh + (16 * J + (lane & 7) + ((lane >> 4) << 3)) * LD64 +
-                                       16 * I + (((lane >> 3) & 1) << 3)),
-                              af[0], af[1], af[2], af[3]);
-                    // B = A_RJ^T as [k=m][n=r] from A_RJ stored (swizzled) [r][m]
-                    const int bn = 16 * R + (lane & 7) + ((lane >> 4) << 3);
-                    const int bkk = 16 * J + (((lane >> 3) & 1) << 3);
-                    ldsm_x4(smem_u32(akh + sw128(bn, bkk, C)), bf[0], bf[1], bf[2], bf[3]);
-                    mma16816(xa[0], af, bf[0], bf[1]);
-                    mma16816(xa[1], af, bf[2], bf[3]);
-                }
-                const uint32_t xf[4] = {pack_h2(-xa[0][0], -xa[0][1]), pack_h2(-xa[0][2], -xa[0][3]),
-                                        pack_h2(-xa[1][0], -xa[1][1]), pack_h2(-xa[1][2], -xa[1][3])};
-                uint32_t tb[4];
-                ldsm_x4(smem_u32(tmh + bnk_off(lane, 16 * R, 16 * R, LD64)), tb[0], tb[1], tb[2], tb[3]);
-                float ta[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-                mma16816(ta[0], xf, tb[0], tb[1]);
-                mma16816(ta[1], xf, tb[2], tb[3]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = 16 * I + g8 + ((e >> 1) << 3);
-                        const int r = 16 * R + 8 * nt + 2 * tig + (e & 1);
-                        tmh[r * LD64 + i] = __float2half_rn(ta[nt][e]);
-                    }
-            }
-            __syncthreads();
-        }
-
-        // ---------------- S2: D^T = (beta X)^T T^T  (mma.sync; T lower triangular: k-blocks <= qw/2)
-        {
-            const int mt = warp & 1, qw = warp >> 1, rblk = qw >> 1;
-            float dacc[4] = {0.f, 0.f, 0.f, 0.f};
-            const int brow = (8 * qw + (lane & 7)) * LD64 + (((lane >> 3) & 1) << 3);
-            for (int ks = 0; ks <= rblk; ++ks) {
-                uint32_t af[4], bt[2];
-                ldsm_x4(smem_u32(xt + a_off(lane, 16 * mt, 16 * ks, LD64)), af[0], af[1], af[2], af[3]);
-                ldsm_x2(smem_u32(tmh + brow + 16 * ks), bt[0], bt[1]);
-                mma16816(dacc, af, bt[0], bt[1]);
-            }
-            const int r = 8 * qw + 2 * tig;
-            const int v0 = 16 * mt + g8;
-            *reinterpret_cast<uint32_t *>(dt + sw128(v0, r, VT)) = pack_h2(dacc[0], dacc[1]);
-            *reinterpret_cast<uint32_t *>(dt + sw128(v0 + 8, r, VT)) = pack_h2(dacc[2], dacc[3]);
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // ---------------- MMA S3: h += K^^T D ; D1[64..127] += A_qk D  (one tcgen05 batch)
-        if (tid == 0) {
+        Tout *out = static_cast<Tout *>(a.out);
+        int ci = 0;
+        for (int64_t t0 = bos; t0 < eos; t0 += C, ++ci) {
+            const int len = (int)((eos - t0) < C ? (eos - t0) : C);
+            const int s = ci & 1, par = ci & 1;
+            if (!mbar_wait(bar(Bar::ready), par)) failed = true;
+            if (bar_red_or(kBarStep, kGroup, failed)) { failed = true; break; }
             tc_fence_after();
-#pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks)
-                umma_f16(tH, sw128_kdesc(smem_u32(kht), ks, KD), sw128_kdesc(smem_u32(dt), ks, VT),
-                         kIdescM128N32, 1u);
-            // A = [A_kk (rows 0..63, lands in the consumed X rows); A_qk (rows 64..127)]
-#pragma unroll
-            for (int ks = 0; ks < C / 16; ++ks)
-                umma_f16(tD1, sw128_kdesc(smem_u32(akh), ks, 2 * C), sw128_kdesc(smem_u32(dt), ks, VT),
-                         kIdescM128N32, 1u);
-            umma_commit(mbar_mma);
-        }
-        if (!mbar_wait(mbar_mma, mma_parity)) failed = true;
-        mma_parity ^= 1u;
-        tc_fence_after();
-        if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {   // rows 64..127 of D1: o
-            const int r = 32 * (warp & 1) + lane, half = warp >> 2;
-            float ov[16];
-            tmem_ld16(tD1 + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * half, ov);
-            if (r < len) store_row16(out + ((t0 + r) * H + h) * VD + vt * VT + 16 * half, ov, a.scale);
-        }
-        tc_fence_before();
-        if (__syncthreads_or(failed)) { failed = true; break; }
-    }
 
-    if (failed) {
-        // error marker: NaN state; copies or MMAs still in flight get one more bounded wait
-        mbar_wait(mbar, load_parity);
-        mbar_wait(mbar_a, a_parity);
-        mbar_wait(mbar_mma, mma_parity);
-    }
-    if (fin && state_warp) {
-        tc_fence_after();
-        float hv[16];
-        tmem_ld16(tH + lane_off + 16 * hc, hv);
+            // ---------------- fp16 copy (2^m h)^T for S1, then h <- Diag(2^G_last) h
+            {
+                float hv[16];
+                tmem_ld16(tH + lane_off + 16 * hc, hv);
+                const float p = pm_s(s)[sc], d = dec_s(s)[sc];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float4 x = make_float4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
-            if (failed) x = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
-                                        __int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
-            *reinterpret_cast<float4 *>(fin + (int64_t)sc * VD + vt * VT + 16 * hc + 4 * j) = x;
+                for (int v = 0; v < 16; ++v) {
+                    ht[sw128(16 * hc + v, sc, VT)] = __float2half_rn(p * hv[v]);
+                    hv[v] *= d;
+                }
+                tmem_st16(tH + lane_off + 16 * hc, hv);
+                fence_proxy_async_smem();
+                tc_fence_before();
+            }
+            named_bar_sync(kBarStep, kGroup);
+
+            // ---------------- MMA S1: D1 = [a_k; a_q] (2^m h) = [K~ h; Q~ h]
+            if (tid == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < KD / 16; ++ks)
+                    umma_f16(tD1, sw128_kdesc(smem_u32(aop), ks, 2 * C), sw128_kdesc(smem_u32(ht), ks, VT),
+                             kIdescM128N32, ks > 0);
+                umma_commit(bar(Bar::s1));
+            }
+            __half *tmh = reinterpret_cast<__half *>(sm + Smem::tm);
+            const __half *akh = akh_s(s);
+            // ---------------- T = (I + A_kk)^-1: the diagonal blocks (inverted by the operand
+            //                  group) into T (warps 2, 3, 6, 7), then the column blocks
+            //                  0, 1, 2 below them (warps 2, 3, 6)
+            if (warp & 2) {
+                const int e = ((warp >> 2) << 6) | ((warp & 1) << 5) | lane;   // 0..127, 16 B each
+                const int R = e >> 5, rr = (e >> 1) & 15, hf = e & 1;
+                *reinterpret_cast<uint4 *>(tmh + (16 * R + rr) * LD64 + 16 * R + 8 * hf) =
+                    *reinterpret_cast<const uint4 *>(tdg_s(s) + (16 * R + rr) * 16 + 8 * hf);
+            }
+            // ---------------- X = beta (v - K~ h) from rows 0..63 of D1 (warps 0, 1, 4, 5)
+            if ((warp & 2) == 0) {
+                if (!mbar_wait(bar(Bar::s1), par)) failed = true;
+                tc_fence_after();
+                const int r = 32 * (warp & 1) + lane, half = warp >> 2;
+                float xv[16];
+                tmem_ld16(tD1 + lane_off + 16 * half, xv);
+                const float b = beta_s(s)[r];
+                const uint4 *vrow = reinterpret_cast<const uint4 *>(vs_s(s) + r * VT + 16 * half);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint4 w = vrow[j];
+                    const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&w);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float2 vv = __bfloat1622float2(p2[u]);
+                        const int v = 8 * j + 2 * u;
+                        xt[(16 * half + v) * LD64 + r] = __float2half_rn(b * (vv.x - xv[v]));
+                        xt[(16 * half + v + 1) * LD64 + r] = __float2half_rn(b * (vv.y - xv[v + 1]));
+                    }
+                }
+                tc_fence_before();
+            }
+            named_bar_sync(kBarStep, kGroup);
+            if (warp == 2 || warp == 3 || warp == 6) solve_column_block(akh, tmh, warp == 6 ? 2 : warp - 2, lane);
+            named_bar_sync(kBarStep, kGroup);
+
+            // ---------------- S2: D^T = (beta X)^T T^T  (mma.sync; T lower triangular: k-blocks <= qw/2)
+            {
+                const int mt = warp & 1;
+#pragma unroll
+                for (int jq = 0; jq < 2; ++jq) {
+                    const int qw = (warp >> 1) + 4 * jq, rblk = qw >> 1;
+                    float dk[4][4];   // one accumulator per k-block (no chained mma)
+                    const int brow = (8 * qw + (lane & 7)) * LD64 + (((lane >> 3) & 1) << 3);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        dk[ks][0] = dk[ks][1] = dk[ks][2] = dk[ks][3] = 0.f;
+                        if (ks <= rblk) {
+                            uint32_t af[4], bt[2];
+                            ldsm_x4(smem_u32(xt + a_off(lane, 16 * mt, 16 * ks, LD64)), af[0], af[1], af[2], af[3]);
+                            ldsm_x2(smem_u32(tmh + brow + 16 * ks), bt[0], bt[1]);
+                            mma16816(dk[ks], af, bt[0], bt[1]);
+                        }
+                    }
+                    float dacc[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dacc[e] = (dk[0][e] + dk[1][e]) + (dk[2][e] + dk[3][e]);
+                    const int r = 8 * qw + 2 * tig;
+                    const int v0 = 16 * mt + g8;
+                    *reinterpret_cast<uint32_t *>(dt + sw128(v0, r, VT)) = pack_h2(dacc[0], dacc[1]);
+                    *reinterpret_cast<uint32_t *>(dt + sw128(v0 + 8, r, VT)) = pack_h2(dacc[2], dacc[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(kBarStep, kGroup);
+
+            // ---------------- MMA S3: h += K^^T D ; D1[64..127] += A_qk D  (one tcgen05 batch)
+            if (tid == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks)
+                    umma_f16(tH, sw128_kdesc(smem_u32(kht_s(s)), ks, KD), sw128_kdesc(smem_u32(dt), ks, VT),
+                             kIdescM128N32, 1u);
+                // A = [A_kk (rows 0..63, lands in the consumed X rows); A_qk (rows 64..127)]
+#pragma unroll
+                for (int ks = 0; ks < C / 16; ++ks)
+                    umma_f16(tD1, sw128_kdesc(smem_u32(akh_s(s)), ks, 2 * C), sw128_kdesc(smem_u32(dt), ks, VT),
+                             kIdescM128N32, 1u);
+                umma_commit(bar(Bar::s3));
+            }
+            if (!mbar_wait(bar(Bar::s3), par)) failed = true;
+            tc_fence_after();
+            if (warp & 2) {   // rows 64..127 of D1: o (warps 2, 3, 6, 7)
+                const int r = 32 * (warp & 1) + lane, half = warp >> 2;
+                float ov[16];
+                tmem_ld16(tD1 + lane_off + 16 * half, ov);
+                if (r < len) store_row16(out + ((t0 + r) * H + h) * VD + vt * VT + 16 * half, ov, a.scale);
+            }
+            tc_fence_before();
+            // slot s and the step buffers are consumed
+            if (bar_red_or(kBarStep, kGroup, failed)) { failed = true; break; }
+            if (tid == 0) mbar_arrive(bar(Bar::free0 + s));
+        }
+        if (failed) {   // MMAs still in flight get one more bounded wait
+            mbar_wait(bar(Bar::s1), ci & 1);
+            mbar_wait(bar(Bar::s3), ci & 1);
+        }
+        if (fin) {   // error marker: NaN state
+            tc_fence_after();
+            float hv[16];
+            tmem_ld16(tH + lane_off + 16 * hc, hv);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float4 x = make_float4(hv[4 * j], hv[4 * j + 1], hv[4 * j + 2], hv[4 * j + 3]);
+                if (failed) x = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
+                                            __int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+                *reinterpret_cast<float4 *>(fin + (int64_t)sc * VD + vt * VT + 16 * hc + 4 * j) = x;
+            }
         }
     }
     tc_fence_before();
