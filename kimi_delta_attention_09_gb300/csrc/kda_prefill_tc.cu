@@ -82,8 +82,7 @@ struct Smem {
     static constexpr int beta = vs + 2 * C * VT * 2;         // x2 f32 [64]
     static constexpr int dec = beta + 2 * C * 4;             // x2 f32 [128] 2^G_last
     static constexpr int pm = dec + 2 * KD * 4;              // x2 f32 [128] 2^m
-    static constexpr int tdg = pm + 2 * KD * 4;              // x2 f16 T_RR [4][16][16] (diagonal blocks)
-    static constexpr int bars = tdg + 2 * 4 * 16 * 16 * 2;             // u64 mbarriers (see Bar)
+    static constexpr int bars = pm + 2 * KD * 4;              // u64 mbarriers (see Bar)
     static constexpr int tmem = bars + 8 * 8;                // u32 tensor-memory base
     static constexpr int flag = tmem + 4;                    // int: exact path for this chunk
     static constexpr int aop = (flag + 4 + 1023) / 1024 * 1024;   // SW128 [a_k; a_q] 128 x 128
@@ -458,9 +457,9 @@ __device__ __noinline__ void exact_intra_chunk(unsigned char *sm, int gtid, cons
 // column j of block R; once T[m][j] is final, every row below it is updated,
 //     T[r][j] -= A[r][m] T[m][j]    (r > m),
 // so the dependent chain is one multiply-add per step.  Columns m, m + 1 of A are
-// read as one 4-byte broadcast per row.  Written to tdg[R][16][16] (fp16) with its
-// zeros and unit diagonal.
-__device__ __forceinline__ void invert_diag_blocks(const __half *akh, __half *tdg, int P, int lane)
+// read as one 4-byte broadcast per row.  Written to T (fp16) with its zeros and unit
+// diagonal.
+__device__ __forceinline__ void invert_diag_blocks(const __half *akh, __half *tmh, int P, int lane)
 {
     const int j = lane & 15, R = 2 * P + (lane >> 4);
     float col[16];
@@ -479,7 +478,7 @@ __device__ __forceinline__ void invert_diag_blocks(const __half *akh, __half *td
         for (int r = m + 2; r < 16; ++r) col[r] -= am[r].y * col[m + 1];
     }
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) tdg[(16 * R + rr) * 16 + j] = __float2half_rn(col[rr]);
+    for (int rr = 0; rr < 16; ++rr) tmh[(16 * R + rr) * LD64 + 16 * R + j] = __float2half_rn(col[rr]);
 }
 
 // T_RI (R > I) of column block I, top to bottom, by ONE warp (no barrier between the
@@ -560,7 +559,6 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
     auto beta_s = [&](int s) { return reinterpret_cast<float *>(sm + Smem::beta) + s * C; };
     auto dec_s = [&](int s) { return reinterpret_cast<float *>(sm + Smem::dec) + s * KD; };
     auto pm_s = [&](int s) { return reinterpret_cast<float *>(sm + Smem::pm) + s * KD; };
-    auto tdg_s = [&](int s) { return reinterpret_cast<__half *>(sm + Smem::tdg) + s * 4 * 16 * 16; };
     auto kht_s = [&](int s) { return reinterpret_cast<__half *>(sm + Smem::kht) + s * KD * C; };
     auto akh_s = [&](int s) { return reinterpret_cast<__half *>(sm + Smem::akh) + s * 2 * C * C; };
     auto bar = [&](int b) { return smem_u32(sm + Smem::bars + 8 * b); };
@@ -739,16 +737,9 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
                     *reinterpret_cast<uint4 *>(dst + sw128(r, c0 + 8 * t, C)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
                 tc_fence_before();
-                // diagonal blocks of T: warp 8 stored A_kk rows 0..31 x columns 0..31 (blocks 0, 1),
-                // warp 13 rows 32..63 x columns 32..63 (blocks 2, 3)
-                if (warp == 8 || warp == 13) {
-                    __syncwarp();
-                    invert_diag_blocks(akh, tdg_s(s), warp == 13, lane);
-                }
             } else {
                 exact_intra_chunk(sm, gtid, bs, akh, aqk, kht);
                 named_bar_sync(kBarPrep, kGroup);
-                if (warp == 8 || warp == 13) invert_diag_blocks(akh, tdg_s(s), warp == 13, lane);
                 if (warp == kLoadWarp && t0 + C < eos) {
                     const int64_t t1 = t0 + C;
                     issue_chunk_loads(sm, a, maps, t1, (int)((eos - t1) < C ? (eos - t1) : C), h, vt, lane);
@@ -822,15 +813,10 @@ kda_prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ TmaMaps maps)
             }
             __half *tmh = reinterpret_cast<__half *>(sm + Smem::tm);
             const __half *akh = akh_s(s);
-            // ---------------- T = (I + A_kk)^-1: the diagonal blocks (inverted by the operand
-            //                  group) into T (warps 2, 3, 6, 7), then the column blocks
-            //                  0, 1, 2 below them (warps 2, 3, 6)
-            if (warp & 2) {
-                const int e = ((warp >> 2) << 6) | ((warp & 1) << 5) | lane;   // 0..127, 16 B each
-                const int R = e >> 5, rr = (e >> 1) & 15, hf = e & 1;
-                *reinterpret_cast<uint4 *>(tmh + (16 * R + rr) * LD64 + 16 * R + 8 * hf) =
-                    *reinterpret_cast<const uint4 *>(tdg_s(s) + (16 * R + rr) * 16 + 8 * hf);
-            }
+            // ---------------- T = (I + A_kk)^-1: the diagonal blocks (warps 2, 3, while S1 runs
+            //                  and warps 0, 1, 4, 5 form X), then the column blocks 0, 1, 2
+            //                  below them (warps 2, 3, 6)
+            if (warp == 2 || warp == 3) invert_diag_blocks(akh, tmh, warp - 2, lane);
             // ---------------- X = beta (v - K~ h) from rows 0..63 of D1 (warps 0, 1, 4, 5)
             if ((warp & 2) == 0) {
                 if (!mbar_wait(bar(Bar::s1), par)) failed = true;
