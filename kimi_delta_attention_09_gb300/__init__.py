@@ -9,8 +9,8 @@ pointers; importing the op functions raises if the library is missing.
 """
 from __future__ import annotations
 
-__all__ = ["chunk_prefill", "chunk_prefill_paged", "recurrent_decode", "kda_chunk_prefill",
-           "kda_chunk_prefill_paged", "kda_recurrent_decode"]
+__all__ = ["chunk_prefill", "chunk_prefill_paged", "chunk_prefill_from_host", "recurrent_decode",
+           "kda_chunk_prefill", "kda_chunk_prefill_paged", "kda_recurrent_decode"]
 
 
 def __getattr__(name):
@@ -73,3 +73,88 @@ def recurrent_decode(q, k, v, g, beta, state_pool, state_idx, scale=None, out_dt
     out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
     _native.kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out, stream)
     return out
+
+
+def chunk_prefill_from_host(q, k, v, g, beta, scale=None, init_state=None, cu_seqlens=None,
+                            out_dtype=None, segments: int = 4, device=None, buffers=None):
+    """Chunked prefill of HOST (pinned) inputs, returning HOST outputs.
+
+    The packed token range is cut into ``segments`` pieces on chunk boundaries; the
+    host-to-device copy of piece s + 1 and the device-to-host copy of the output of
+    piece s - 1 overlap the prefill of piece s (three CUDA streams).  Each piece is one
+    ``kda_chunk_prefill`` call over the tokens of every sequence that fall in it, with
+    the per-sequence states carried from piece to piece in place -- a prefill split at
+    any token and continued from the carried state equals the unsplit one.
+
+    q, k, v, g, beta, init_state, cu_seqlens are CPU tensors (pinned memory gives
+    asynchronous copies).  Returns ``(out, final_state, buffers)``: pinned CPU tensors,
+    valid once the current stream of ``device`` has been synchronised, and the working
+    buffers (device tensors, pinned output tensors, streams), which a later call with
+    the same shapes, cu_seqlens and segments may pass back as ``buffers``; that call
+    then allocates nothing and overwrites the returned outputs.
+    """
+    import torch
+    from . import _native
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    T, H, K = q.shape
+    V = v.shape[-1]
+    if scale is None:
+        scale = K ** -0.5
+    if cu_seqlens is None:
+        cu_seqlens = torch.tensor([0, T], dtype=torch.int32)
+    N = cu_seqlens.numel() - 1
+    chunk = 64
+    nch = (T + chunk - 1) // chunk
+    segments = max(1, min(int(segments), nch))
+    bounds = [chunk * ((nch * s) // segments) for s in range(segments)] + [T]
+    if buffers is None:
+        # per-piece cu_seqlens (each sequence clipped to the piece), one pinned host block
+        # whose rows are padded to 16 bytes (the C ABI wants 16-byte aligned pointers)
+        cu = cu_seqlens.to(torch.int64)
+        row = (N + 1 + 3) // 4 * 4
+        cu_seg = torch.zeros(segments, row, dtype=torch.int32)
+        for s_, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
+            cu_seg[s_, :N + 1] = (cu - b0).clamp(0, b1 - b0).to(torch.int32)
+        buffers = {
+            "q": torch.empty(q.shape, dtype=q.dtype, device=device),
+            "k": torch.empty(k.shape, dtype=k.dtype, device=device),
+            "v": torch.empty(v.shape, dtype=v.dtype, device=device),
+            "g": torch.empty(g.shape, dtype=g.dtype, device=device),
+            "beta": torch.empty(beta.shape, dtype=beta.dtype, device=device),
+            "cu": cu_seg.to(device),
+            "out": torch.empty(v.shape, dtype=out_dtype or v.dtype, device=device),
+            "state": torch.empty(N, H, K, V, dtype=torch.float32, device=device),
+            "hout": torch.empty(v.shape, dtype=out_dtype or v.dtype).pin_memory(),
+            "hfin": torch.empty(N, H, K, V, dtype=torch.float32).pin_memory(),
+            "copy": torch.cuda.Stream(device), "back": torch.cuda.Stream(device),
+            "events": [torch.cuda.Event() for _ in range(2 * segments)],
+        }
+    d = buffers
+    hout, hfin = d["hout"], d["hfin"]
+    main = torch.cuda.current_stream(device)
+    cs, bs = d["copy"], d["back"]
+    cs.wait_stream(main)
+    bs.wait_stream(main)
+    with torch.cuda.stream(cs):
+        if init_state is None:
+            d["state"].zero_()
+        else:
+            d["state"].copy_(init_state, non_blocking=True)
+        for s, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
+            for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+                d[name][b0:b1].copy_(t[b0:b1], non_blocking=True)
+            d["events"][s].record(cs)
+    for s, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
+        main.wait_event(d["events"][s])
+        _native.kda_chunk_prefill(d["q"][b0:b1], d["k"][b0:b1], d["v"][b0:b1], d["g"][b0:b1],
+                                  d["beta"][b0:b1], scale, d["state"], d["cu"][s, :N + 1],
+                                  d["out"][b0:b1], d["state"], main)
+        ev = d["events"][segments + s]
+        ev.record(main)
+        bs.wait_event(ev)
+        with torch.cuda.stream(bs):
+            hout[b0:b1].copy_(d["out"][b0:b1], non_blocking=True)
+    with torch.cuda.stream(bs):
+        hfin.copy_(d["state"], non_blocking=True)
+    main.wait_stream(bs)
+    return hout, hfin, buffers

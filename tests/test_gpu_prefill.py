@@ -215,3 +215,36 @@ def test_paged_prefill_then_paged_decode():
     assert rel_err(torch.cat(outs), ref_out) <= TOL["bf16"]
     assert rel_err(pool[3].cpu(), ref_fin[0]) <= TOL["bf16"]
     assert torch.equal(pool[:3].cpu(), torch.zeros(3, H, 128, 128))
+
+
+# ------------------------------------------------------------ host-staged (pipelined) prefill
+
+@pytest.mark.parametrize("segments", [1, 3, 4])
+def test_prefill_from_host_matches_oracle(segments):
+    """Host inputs, pieces cut on 64-token boundaries of the packed range (so sequences
+    are split mid-chunk and carried across pieces), nonzero initial states."""
+    import kimi_delta_attention_09_gb300 as kda
+    case = inputs.prefill_case([1, 63, 150, 65, 230], H=2, K=128, V=128, dtype="bf16", seed=73,
+                               init_std=0.02)
+    pin = [x.pin_memory() for x in (case.q, case.k, case.v, case.g, case.beta)]
+    out, fin, _ = kda.chunk_prefill_from_host(*pin, case.scale, case.init_state.pin_memory(),
+                                              case.cu_seqlens, out_dtype=torch.float32,
+                                              segments=segments)
+    torch.cuda.synchronize()
+    ref_out, ref_fin = oracle_prefill(case)
+    assert rel_err(out, ref_out) <= TOL["bf16"]
+    assert rel_err(fin, ref_fin) <= TOL["bf16"]
+
+
+def test_prefill_from_host_reuses_buffers():
+    """Two calls in a row with the first call's device buffers give the same result."""
+    import kimi_delta_attention_09_gb300 as kda
+    case = inputs.prefill_case([300], H=2, K=128, V=128, dtype="bf16", seed=74)
+    pin = [x.pin_memory() for x in (case.q, case.k, case.v, case.g, case.beta)]
+    o1, f1, bufs = kda.chunk_prefill_from_host(*pin, case.scale, None, case.cu_seqlens, segments=3)
+    torch.cuda.synchronize()
+    o1, f1 = o1.clone(), f1.clone()
+    o2, f2, _ = kda.chunk_prefill_from_host(*pin, case.scale, None, case.cu_seqlens, segments=3,
+                                            buffers=bufs)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(f1, f2)
