@@ -17,6 +17,10 @@
  *                            chunk (64 tokens), from an optional initial state;
  *                            returns the outputs and the final state per sequence
  *                            (the state carried into decode, PR #113).
+ *   kda_chunk_prefill_ws  -- the same prefill with a caller workspace, through which
+ *                            the four value-tile CTAs of a head share the per-chunk
+ *                            operands instead of each building them (faster; same
+ *                            result up to fp32 rounding).
  *   kda_chunk_prefill_paged -- the same prefill with the initial and final states in
  *                            paged pool slots selected per sequence (in place).
  *   kda_recurrent_decode  -- one token per sequence against the state held in a
@@ -57,7 +61,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 1
+#define KDA_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define KDA_API __attribute__((visibility("default")))
@@ -128,6 +132,46 @@ KDA_API int kda_chunk_prefill(const void *q, const void *k, const void *v,
                               int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
                               int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
                               int32_t out_dtype, void *stream);
+
+/*
+ * Bytes of workspace kda_chunk_prefill_ws needs for these sizes on the CURRENT device
+ * (the ring of per-chunk operand records of the clusters that can be resident at
+ * once: at most (SMs / 4) x 8 x 66,816 bytes, ~20 MB on a 152-SM GPU, whatever
+ * num_seqs is).  0 when the call needs none: num_seqs == 0, or shapes that do not run
+ * on the shared-operand kernel (dtype fp32, or K or V != 128).
+ */
+KDA_API size_t kda_chunk_prefill_workspace_bytes(int32_t num_seqs, int32_t num_heads,
+                                                 int32_t head_dim_k, int32_t head_dim_v,
+                                                 int32_t dtype);
+
+/*
+ * kda_chunk_prefill with a caller-owned device workspace.
+ *
+ * Same operation, arguments, conventions and results as kda_chunk_prefill (vllm.cpp PR
+ * #110, commit description; PR #113, commit body); only the schedule differs: the four
+ * CTAs that hold the 32-column value tiles of one (sequence, head) form a thread-block
+ * cluster, each builds the intra-chunk operands (gate cumsum, decayed factors, A_kk,
+ * A_qk and the triangular inverse) of every fourth chunk, and all four read them back
+ * through a ring in `workspace`.  Outputs agree with kda_chunk_prefill up to fp32
+ * summation order.
+ *
+ *   workspace        device pointer, 16-byte aligned, at least
+ *                    kda_chunk_prefill_workspace_bytes(num_seqs, num_heads, head_dim_k,
+ *                    head_dim_v, dtype) bytes (queried on the device that runs the call);
+ *                    may be NULL when that is 0.  Contents need no initialisation and
+ *                    are garbage afterwards.  It must not overlap any other argument
+ *                    (KDA_ERR_ALIAS), and two calls in flight at once need two workspaces.
+ *   workspace_bytes  its size; smaller than required -> KDA_ERR_INVALID_ARG.
+ * Every other argument as for kda_chunk_prefill.
+ */
+KDA_API int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
+                                 const float *g, const float *beta, float scale,
+                                 const float *init_state, const int32_t *cu_seqlens,
+                                 void *out, float *final_state,
+                                 int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
+                                 int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                                 int32_t out_dtype, void *workspace, size_t workspace_bytes,
+                                 void *stream);
 
 /*
  * Chunked prefill whose per-sequence states live in paged pool slots.

@@ -19,10 +19,11 @@ KDA_ERR_ALIAS = -3
 KDA_ERR_CUDA = -4
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
-            "kda_chunk_prefill", "kda_chunk_prefill_paged", "kda_recurrent_decode")
+            "kda_chunk_prefill", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_ws",
+            "kda_chunk_prefill_paged", "kda_recurrent_decode")
 
 
 class KdaError(RuntimeError):
@@ -47,6 +48,11 @@ def _load() -> ctypes.CDLL:
     lib.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
                                       i64, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_chunk_prefill.restype = ctypes.c_int
+    lib.kda_chunk_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.kda_chunk_prefill_workspace_bytes.restype = ctypes.c_size_t
+    lib.kda_chunk_prefill_ws.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
+                                         i64, i32, i32, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]
+    lib.kda_chunk_prefill_ws.restype = ctypes.c_int
     lib.kda_chunk_prefill_paged.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
                                             i64, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_chunk_prefill_paged.restype = ctypes.c_int
@@ -128,6 +134,48 @@ def kda_chunk_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out, fina
                                T, N, H, K, V, _dtype_code(q), _dtype_code(out),
                                _stream_handle(stream))
     _check("kda_chunk_prefill", rc)
+
+
+def kda_chunk_prefill_workspace_bytes(num_seqs: int, num_heads: int, head_dim_k: int,
+                                      head_dim_v: int, dtype) -> int:
+    """Workspace bytes ``kda_chunk_prefill_ws`` needs on the current device (``dtype``: a
+    torch dtype of q/k/v)."""
+    import torch
+    code = KDA_DTYPE_BF16 if dtype == torch.bfloat16 else KDA_DTYPE_F32
+    return int(lib.kda_chunk_prefill_workspace_bytes(int(num_seqs), int(num_heads), int(head_dim_k),
+                                                     int(head_dim_v), code))
+
+
+def kda_chunk_prefill_ws(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
+                         workspace, stream=None) -> None:
+    """Enqueue ``kda_chunk_prefill_ws``: as ``kda_chunk_prefill`` plus ``workspace``, a
+    contiguous CUDA tensor (any dtype) of at least ``kda_chunk_prefill_workspace_bytes``
+    bytes, or None when that is 0."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out),
+                    ("cu_seqlens", cu_seqlens), ("init_state", init_state),
+                    ("final_state", final_state), ("workspace", workspace)):
+        if t is not None:
+            _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _need(k.shape == q.shape and g.shape == q.shape, "q, k, g must be [T, H, K]")
+    _need(v.shape[:2] == (T, H) and out.shape == v.shape, "v, out must be [T, H, V]")
+    _need(beta.shape == (T, H), "beta must be [T, H]")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v must share one dtype")
+    import torch
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g, beta must be fp32")
+    _need(cu_seqlens.dtype == torch.int32, "cu_seqlens must be int32")
+    for s in (init_state, final_state):
+        if s is not None:
+            _need(s.dtype == torch.float32 and tuple(s.shape) == (N, H, K, V),
+                  "states must be fp32 [N, H, K, V]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.kda_chunk_prefill_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                  _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                  T, N, H, K, V, _dtype_code(q), _dtype_code(out), _ptr(workspace),
+                                  ws_bytes, _stream_handle(stream))
+    _check("kda_chunk_prefill_ws", rc)
 
 
 def kda_chunk_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens, out,

@@ -47,33 +47,13 @@ int launch_prefill(const kda::PrefillArgs &a, void *stream)
                                                : kda::launch_prefill_simt(a, st));
 }
 
-}  // namespace
-
-extern "C" {
-
-int kda_abi_version(void) { return KDA_ABI_VERSION; }
-
-const char *kda_status_string(int status)
-{
-    switch (status) {
-    case KDA_OK: return "KDA_OK";
-    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
-    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
-    case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS";
-    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
-    default: return "KDA_ERR_UNKNOWN";
-    }
-}
-
-int kda_last_cuda_error(void) { return g_last_cuda_error; }
-
-int kda_chunk_prefill(const void *q, const void *k, const void *v,
-                      const float *g, const float *beta, float scale,
-                      const float *init_state, const int32_t *cu_seqlens,
-                      void *out, float *final_state,
-                      int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
-                      int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                      int32_t out_dtype, void *stream)
+// Validation shared by kda_chunk_prefill and kda_chunk_prefill_ws: fills `a` and the
+// byte ranges of every input and output (for the workspace alias check).
+int check_prefill(const void *q, const void *k, const void *v, const float *g, const float *beta,
+                  float scale, const float *init_state, const int32_t *cu_seqlens, void *out,
+                  float *final_state, int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
+                  int32_t head_dim_k, int32_t head_dim_v, int32_t dtype, int32_t out_dtype,
+                  kda::PrefillArgs &a, Range (&ranges)[9])
 {
     if (total_tokens < 0 || num_seqs < 0 || num_heads < 1 || !std::isfinite(scale))
         return KDA_ERR_INVALID_ARG;
@@ -103,14 +83,88 @@ int kda_chunk_prefill(const void *q, const void *k, const void *v,
         if (overlaps(r_out, r) || overlaps(r_final, r)) return KDA_ERR_ALIAS;
     if (overlaps(r_out, r_init) || overlaps(r_out, r_final)) return KDA_ERR_ALIAS;
     if (overlaps(r_final, r_init) && final_state != init_state) return KDA_ERR_ALIAS;
+    for (int i = 0; i < 6; ++i) ranges[i] = in[i];
+    ranges[6] = r_out;
+    ranges[7] = r_init;
+    ranges[8] = r_final;
 
-    kda::PrefillArgs a{};
+    a = kda::PrefillArgs{};
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
     a.init_state = init_state; a.cu_seqlens = cu_seqlens; a.out = out;
     a.final_state = final_state; a.total_tokens = total_tokens; a.num_seqs = num_seqs;
     a.num_heads = num_heads; a.head_dim_k = head_dim_k; a.head_dim_v = head_dim_v;
     a.dtype = dtype; a.out_dtype = out_dtype;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char *kda_status_string(int status)
+{
+    switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+int kda_last_cuda_error(void) { return g_last_cuda_error; }
+
+int kda_chunk_prefill(const void *q, const void *k, const void *v,
+                      const float *g, const float *beta, float scale,
+                      const float *init_state, const int32_t *cu_seqlens,
+                      void *out, float *final_state,
+                      int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
+                      int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                      int32_t out_dtype, void *stream)
+{
+    kda::PrefillArgs a;
+    Range ranges[9];
+    const int st = check_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
+                                 total_tokens, num_seqs, num_heads, head_dim_k, head_dim_v, dtype,
+                                 out_dtype, a, ranges);
+    if (st != KDA_OK || num_seqs == 0) return st;
     return launch_prefill(a, stream);
+}
+
+size_t kda_chunk_prefill_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
+                                         int32_t head_dim_v, int32_t dtype)
+{
+    if (num_seqs <= 0 || num_heads < 1) return 0;
+    kda::PrefillArgs a{};
+    a.num_seqs = num_seqs; a.num_heads = num_heads; a.head_dim_k = head_dim_k;
+    a.head_dim_v = head_dim_v; a.dtype = dtype;
+    return kda::prefill_rr_workspace_bytes(a);
+}
+
+int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
+                         const float *g, const float *beta, float scale,
+                         const float *init_state, const int32_t *cu_seqlens,
+                         void *out, float *final_state,
+                         int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
+                         int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                         int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    kda::PrefillArgs a;
+    Range ranges[9];
+    const int st = check_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
+                                 total_tokens, num_seqs, num_heads, head_dim_k, head_dim_v, dtype,
+                                 out_dtype, a, ranges);
+    if (st != KDA_OK || num_seqs == 0) return st;
+    const size_t need = kda::prefill_rr_workspace_bytes(a);
+    if (need == 0) return launch_prefill(a, stream);   // shapes without the shared-operand kernel
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
+    const Range r_ws{workspace, (uint64_t)need};
+    for (const Range &r : ranges)
+        if (overlaps(r_ws, r)) return KDA_ERR_ALIAS;
+    return finish(kda::launch_prefill_rr(a, workspace, static_cast<cudaStream_t>(stream)));
 }
 
 int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,

@@ -65,6 +65,10 @@ cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t stream);
 // Chunked prefill on tensor cores (bf16 q/k/v with K = V = 128).
 bool prefill_tc_supported(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
+// Chunked prefill on tensor cores with the per-chunk operands built once per head by a
+// 4-CTA cluster and shared through a caller workspace (same support as the above).
+size_t prefill_rr_workspace_bytes(const PrefillArgs &a);
+cudaError_t launch_prefill_rr(const PrefillArgs &a, void *workspace, cudaStream_t stream);
 // One-token paged decode.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 

@@ -1,0 +1,193 @@
+"""kda_chunk_prefill_ws (per-chunk operands shared across a 4-CTA cluster through a
+workspace) on the GPU against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+from kimi_delta_attention_09_gb300 import inputs
+from _helpers import TOL, cuda, dtype_name, oracle_prefill, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def workspace_for(case):
+    from kimi_delta_attention_09_gb300 import _native
+    n = _native.kda_chunk_prefill_workspace_bytes(case.N, case.H, case.K, case.V, case.q.dtype)
+    return None if n == 0 else torch.empty(n, dtype=torch.uint8, device="cuda")
+
+
+def run_ws(case, init_in_place=False, final=True, out_dtype=torch.float32, workspace=None):
+    from kimi_delta_attention_09_gb300 import _native
+    q, k, v, g, beta = (cuda(x) for x in (case.q, case.k, case.v, case.g, case.beta))
+    cu = cuda(case.cu_seqlens)
+    init = cuda(case.init_state)
+    out = torch.full(v.shape, float("nan"), dtype=out_dtype, device="cuda")
+    fin = None
+    if final:
+        fin = init if (init_in_place and init is not None) else torch.full(
+            (case.N, case.H, case.K, case.V), float("nan"), device="cuda")
+    ws = workspace_for(case) if workspace is None else workspace
+    _native.kda_chunk_prefill_ws(q, k, v, g, beta, case.scale, init, cu, out, fin, ws)
+    torch.cuda.synchronize()
+    return out.cpu(), (None if fin is None else fin.cpu())
+
+
+def check_case(case, heads=None, seqs=None, **kw):
+    out, fin = run_ws(case, **kw)
+    heads = list(range(case.H)) if heads is None else heads
+    seqs = list(range(case.N)) if seqs is None else seqs
+    ref_out, ref_fin = oracle_prefill(case, heads, seqs)
+    tol = TOL[dtype_name(case.q)]
+    rows = np.concatenate([np.arange(int(case.cu_seqlens[n]), int(case.cu_seqlens[n + 1]))
+                           for n in seqs]) if seqs else np.zeros(0, dtype=np.int64)
+    e_out = rel_err(out[rows][:, heads], ref_out[rows]) if rows.size else 0.0
+    e_fin = rel_err(fin[seqs][:, heads], ref_fin)
+    assert e_out <= tol, f"out rel err {e_out:.3e} > {tol}"
+    assert e_fin <= tol, f"final state rel err {e_fin:.3e} > {tol}"
+    return out, fin
+
+
+def test_workspace_size_query():
+    from kimi_delta_attention_09_gb300 import _native
+    n = _native.kda_chunk_prefill_workspace_bytes(1, 32, 128, 128, torch.bfloat16)
+    assert n > 0 and n % 16 == 0
+    # bounded by the resident clusters, not by the number of sequences
+    assert _native.kda_chunk_prefill_workspace_bytes(4096, 32, 128, 128, torch.bfloat16) <= 64 * n
+    assert _native.kda_chunk_prefill_workspace_bytes(1, 32, 128, 128, torch.float32) == 0
+    assert _native.kda_chunk_prefill_workspace_bytes(1, 32, 64, 128, torch.bfloat16) == 0
+    assert _native.kda_chunk_prefill_workspace_bytes(0, 32, 128, 128, torch.bfloat16) == 0
+
+
+def test_ragged_varlen_with_initial_state():
+    """Several chunks, ragged tails (1, 63, 64, 65, 200 tokens), nonzero init."""
+    case = inputs.prefill_case([1, 63, 64, 65, 200], H=3, K=128, V=128, dtype="bf16", seed=160,
+                               init_std=0.02)
+    check_case(case)
+
+
+def test_more_work_items_than_clusters():
+    """80 (sequence, head) items, empty ones included: each persistent cluster walks
+    several items and the record ring wraps many times."""
+    case = inputs.prefill_case([0, 5, 64, 130, 1, 200, 0, 77, 300, 65], H=8, K=128, V=128,
+                               dtype="bf16", seed=161, init_std=0.02)
+    out, fin = check_case(case)
+    for n in (0, 6):   # empty sequences return their initial state
+        assert torch.equal(fin[n], case.init_state[n])
+
+
+def test_final_state_in_place_and_empty_sequences():
+    case = inputs.prefill_case([0, 130, 0, 5], H=2, K=128, V=128, dtype="bf16", seed=162,
+                               init_std=0.05)
+    check_case(case, init_in_place=True)
+
+
+def test_bf16_output_is_the_rounded_fp32_output():
+    case = inputs.prefill_case([1, 64, 130], H=2, K=128, V=128, dtype="bf16", seed=163,
+                               init_std=0.02)
+    o32, f32 = run_ws(case, out_dtype=torch.float32)
+    o16, f16 = run_ws(case, out_dtype=torch.bfloat16)
+    assert torch.equal(o16.view(torch.int16), o32.to(torch.bfloat16).view(torch.int16))
+    assert torch.equal(f16, f32)
+
+
+def test_agrees_with_the_fused_kernel():
+    """Same algebra and precision as kda_chunk_prefill, so the two agree well inside the
+    oracle tolerance; they differ only where an fp16 operand of K^^T rounds differently
+    (built as k 2^(G_last - G) here, as (k 2^(m - G)) 2^(G_last - m) there)."""
+    from kimi_delta_attention_09_gb300 import _native
+    case = inputs.prefill_case([300, 77], H=4, K=128, V=128, dtype="bf16", seed=164,
+                               init_std=0.02)
+    o_ws, f_ws = run_ws(case)
+    q, k, v, g, beta = (cuda(x) for x in (case.q, case.k, case.v, case.g, case.beta))
+    out = torch.empty(v.shape, device="cuda")
+    fin = torch.empty(case.N, case.H, 128, 128, device="cuda")
+    _native.kda_chunk_prefill(q, k, v, g, beta, case.scale, cuda(case.init_state),
+                              cuda(case.cu_seqlens), out, fin)
+    torch.cuda.synchronize()
+    assert rel_err(o_ws, out.cpu().double().numpy()) <= 1e-3
+    assert rel_err(f_ws, fin.cpu().double().numpy()) <= 1e-3
+
+
+def test_two_calls_with_one_workspace():
+    """The workspace needs no initialisation: a second call on the first call's leftovers
+    gives the identical result."""
+    case = inputs.prefill_case([200, 9], H=3, K=128, V=128, dtype="bf16", seed=165,
+                               init_std=0.02)
+    ws = workspace_for(case)
+    ws.fill_(0xFF)
+    o1, f1 = run_ws(case, workspace=ws)
+    o2, f2 = run_ws(case, workspace=ws)
+    assert torch.equal(o1.view(torch.int32), o2.view(torch.int32))
+    assert torch.equal(f1.view(torch.int32), f2.view(torch.int32))
+
+
+def test_strong_gates():
+    """Gates down to -5 per step per channel: the exact-exponential path in the builder."""
+    case = inputs.prefill_case([150], H=2, K=128, V=128, dtype="bf16", seed=166)
+    gen = torch.Generator().manual_seed(166)
+    case.g = (-5.0 * torch.rand(case.g.shape, generator=gen)).float()
+    check_case(case)
+
+
+def test_split_prefill_carries_state():
+    full = inputs.prefill_case([300], H=2, K=128, V=128, dtype="bf16", seed=167, init_std=0.02)
+    T1 = 137
+    a = inputs.PrefillCase(name="a", seed=0, q=full.q[:T1], k=full.k[:T1], v=full.v[:T1],
+                           g=full.g[:T1], beta=full.beta[:T1],
+                           cu_seqlens=torch.tensor([0, T1], dtype=torch.int32),
+                           init_state=full.init_state, scale=full.scale)
+    out_a, fin_a = run_ws(a)
+    b = inputs.PrefillCase(name="b", seed=0, q=full.q[T1:], k=full.k[T1:], v=full.v[T1:],
+                           g=full.g[T1:], beta=full.beta[T1:],
+                           cu_seqlens=torch.tensor([0, 300 - T1], dtype=torch.int32),
+                           init_state=fin_a, scale=full.scale)
+    out_b, fin_b = run_ws(b)
+    ref_out, ref_fin = oracle_prefill(full)
+    assert rel_err(torch.cat([out_a, out_b]), ref_out) <= TOL["bf16"]
+    assert rel_err(fin_b, ref_fin) <= TOL["bf16"]
+
+
+def test_shapes_without_the_cluster_kernel_need_no_workspace():
+    """fp32 inputs and K = 64 run the other kernels; workspace None is accepted."""
+    for dtype, K, V in (("f32", 128, 128), ("bf16", 64, 128)):
+        case = inputs.prefill_case([70, 3], H=2, K=K, V=V, dtype=dtype, seed=168, init_std=0.02)
+        check_case(case)
+
+
+def test_workspace_errors():
+    from kimi_delta_attention_09_gb300 import _native
+    case = inputs.prefill_case([100], H=2, K=128, V=128, dtype="bf16", seed=169)
+    q, k, v, g, beta = (cuda(x) for x in (case.q, case.k, case.v, case.g, case.beta))
+    cu = cuda(case.cu_seqlens)
+    n = _native.kda_chunk_prefill_workspace_bytes(case.N, case.H, 128, 128, torch.bfloat16)
+    out = torch.zeros(v.shape, device="cuda")
+    small = torch.empty(n - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(_native.KdaError) as e:
+        _native.kda_chunk_prefill_ws(q, k, v, g, beta, case.scale, None, cu, out, None, small)
+    assert e.value.status == _native.KDA_ERR_INVALID_ARG
+    with pytest.raises(_native.KdaError) as e:
+        _native.kda_chunk_prefill_ws(q, k, v, g, beta, case.scale, None, cu, out, None, None)
+    assert e.value.status == _native.KDA_ERR_INVALID_ARG
+    big = torch.empty(n + v.numel() * 4, dtype=torch.uint8, device="cuda")
+    lo = n - 4096   # the output overlaps the last 4 KB the call would use
+    out_in_ws = big[lo:lo + v.numel() * 4].view(torch.float32).view(v.shape)
+    with pytest.raises(_native.KdaError) as e:
+        _native.kda_chunk_prefill_ws(q, k, v, g, beta, case.scale, None, cu, out_in_ws, None, big)
+    assert e.value.status == _native.KDA_ERR_ALIAS
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0   # nothing was launched
+
+
+# ------------------------------------------------------------ full-size workloads
+
+def test_single_prompt_workload_sampled_heads():
+    check_case(inputs.single_prompt(), heads=[0, 9, 22, 31])
+
+
+def test_varlen_packed_workload_sampled():
+    case = inputs.varlen_packed()
+    check_case(case, heads=[1, 16, 30], seqs=[0, 4, 6])
+
+
+def test_long_prefill_workload_sampled():
+    check_case(inputs.long_prefill(), heads=[5, 27])
