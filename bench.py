@@ -3,7 +3,8 @@
 
 A step is one pass of the hot path over the single-prompt workload (B=1, H=32,
 T=4096, K=V=128, bf16 q/k/v, fp32 gates/state, zero initial state, final state
-returned): one ``kda_chunk_prefill`` call.  ``value`` is prefill tokens/s over all
+returned): one ``kda_chunk_prefill_ws`` call (the 4-CTA cluster kernel that shares each
+chunk's operands across the value tiles).  ``value`` is prefill tokens/s over all
 ranks; the same run also times the paged-decode workload (256 sequences x 1 token,
 H=32, K=V=128, 1024-slot fp32 pool, 64 steps carrying state in place) and reports
 its state GB/s under "decode".
@@ -212,7 +213,7 @@ def time_steps(fn, steps, warmup, stream, flush_buf, sleep_cycles=200_000):
 
 
 def measure_prefill(args, dev, stream, flush, world):
-    """Device time of kda_chunk_prefill on the single-prompt workload."""
+    """Device time of kda_chunk_prefill_ws on the single-prompt workload."""
     import torch
     from kimi_delta_attention_09_gb300 import _native, inputs
     case = inputs.single_prompt()
@@ -222,9 +223,11 @@ def measure_prefill(args, dev, stream, flush, world):
     cu = case.cu_seqlens.to(dev)
     out = torch.empty_like(v)                       # bf16 output
     fin = torch.empty(case.N, H, K, V, dtype=torch.float32, device=dev)
+    ws = torch.empty(_native.kda_chunk_prefill_workspace_bytes(case.N, H, K, V, q.dtype),
+                     dtype=torch.uint8, device=dev)
 
     def step():
-        _native.kda_chunk_prefill(q, k, v, g, beta, case.scale, None, cu, out, fin, stream)
+        _native.kda_chunk_prefill_ws(q, k, v, g, beta, case.scale, None, cu, out, fin, ws, stream)
 
     barrier(world)
     with ClockSampler(gpu_id_for(dev.index)) as clk:
@@ -328,10 +331,10 @@ def run_ours(args, rank, world, local):
                         "gb_per_s_algorithmic": round(p_gbs, 1),
                         "ms_per_call": round(p_ms, 5), "ms_min": round(min(ptimes), 5),
                         "algorithmic_bytes": p_bytes, "algorithmic_flops": p_flops},
-            "roofline": {"bound": "hbm", "kernel": "kda_prefill_tc_kernel",
+            "roofline": {"bound": "hbm", "kernel": "kda_prefill_rr_kernel",
                          "achieved": round(p_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                          "frac": round(p_gbs / peak_hbm, 4), "peak_source": peaks["source"],
-                         "traffic": traffic.get("prefill_single_prompt")},
+                         "traffic": traffic.get("prefill_rr_single_prompt")},
             "clocks": clocks,
         })
         if args.only == "all":

@@ -10,29 +10,56 @@ pointers; importing the op functions raises if the library is missing.
 from __future__ import annotations
 
 __all__ = ["chunk_prefill", "chunk_prefill_paged", "chunk_prefill_from_host", "recurrent_decode",
-           "kda_chunk_prefill", "kda_chunk_prefill_paged", "kda_recurrent_decode"]
+           "prefill_workspace", "kda_chunk_prefill", "kda_chunk_prefill_ws",
+           "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_paged", "kda_recurrent_decode"]
 
 
 def __getattr__(name):
-    if name in ("kda_chunk_prefill", "kda_chunk_prefill_paged", "kda_recurrent_decode",
-                "KdaError"):
+    if name in ("kda_chunk_prefill", "kda_chunk_prefill_ws", "kda_chunk_prefill_workspace_bytes",
+                "kda_chunk_prefill_paged", "kda_recurrent_decode", "KdaError"):
         from . import _native
         return getattr(_native, name)
     raise AttributeError(name)
 
 
+_WORKSPACES = {}
+
+
+def prefill_workspace(num_seqs, num_heads, head_dim_k, head_dim_v, dtype, device=None,
+                      stream=None):
+    """The device workspace ``kda_chunk_prefill_ws`` needs for these sizes (None when it
+    needs none), allocated with torch and cached per (device, stream): calls enqueued on
+    one stream run one after another and can share it; calls on different streams get
+    different buffers.  It only grows."""
+    import torch
+    from . import _native
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    n = _native.kda_chunk_prefill_workspace_bytes(num_seqs, num_heads, head_dim_k, head_dim_v, dtype)
+    if n == 0:
+        return None
+    st = torch.cuda.current_stream(dev) if stream is None else stream
+    key = (dev.index, st.cuda_stream)
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < n:
+        ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        _WORKSPACES[key] = ws
+    return ws
+
+
 def chunk_prefill(q, k, v, g, beta, scale=None, init_state=None, cu_seqlens=None,
                   output_final_state: bool = True, final_state=None, out_dtype=None,
-                  stream=None):
+                  stream=None, workspace=None):
     """Chunked KDA prefill of packed sequences (CUDA tensors, layouts of include/kda.h).
 
     Returns ``(out, final_state)``; ``final_state`` is None when not requested.
     Passing ``final_state=init_state`` carries the state in place.  ``out_dtype``
-    defaults to the dtype of ``v``.
+    defaults to the dtype of ``v``.  Runs ``kda_chunk_prefill_ws`` with ``workspace``,
+    or with the cached workspace of ``prefill_workspace`` when None.
     """
     import torch
     from . import _native
     T, H, K = q.shape
+    V = v.shape[-1]
     if scale is None:
         scale = K ** -0.5
     if cu_seqlens is None:
@@ -40,9 +67,11 @@ def chunk_prefill(q, k, v, g, beta, scale=None, init_state=None, cu_seqlens=None
     N = cu_seqlens.numel() - 1
     out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
     if final_state is None and output_final_state:
-        final_state = torch.empty(N, H, K, v.shape[-1], dtype=torch.float32, device=q.device)
-    _native.kda_chunk_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
-                              final_state, stream)
+        final_state = torch.empty(N, H, K, V, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = prefill_workspace(N, H, K, V, q.dtype, q.device, stream)
+    _native.kda_chunk_prefill_ws(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
+                                 final_state, workspace, stream)
     return out, final_state
 
 
@@ -82,7 +111,7 @@ def chunk_prefill_from_host(q, k, v, g, beta, scale=None, init_state=None, cu_se
     The packed token range is cut into ``segments`` pieces on chunk boundaries; the
     host-to-device copy of piece s + 1 and the device-to-host copy of the output of
     piece s - 1 overlap the prefill of piece s (three CUDA streams).  Each piece is one
-    ``kda_chunk_prefill`` call over the tokens of every sequence that fall in it, with
+    ``kda_chunk_prefill_ws`` call over the tokens of every sequence that fall in it, with
     the per-sequence states carried from piece to piece in place -- a prefill split at
     any token and continued from the carried state equals the unsplit one.
 
@@ -124,11 +153,15 @@ def chunk_prefill_from_host(q, k, v, g, beta, scale=None, init_state=None, cu_se
             "cu": cu_seg.to(device),
             "out": torch.empty(v.shape, dtype=out_dtype or v.dtype, device=device),
             "state": torch.empty(N, H, K, V, dtype=torch.float32, device=device),
+            "ws": None,
             "hout": torch.empty(v.shape, dtype=out_dtype or v.dtype).pin_memory(),
             "hfin": torch.empty(N, H, K, V, dtype=torch.float32).pin_memory(),
             "copy": torch.cuda.Stream(device), "back": torch.cuda.Stream(device),
             "events": [torch.cuda.Event() for _ in range(2 * segments)],
         }
+        n_ws = _native.kda_chunk_prefill_workspace_bytes(N, H, K, V, q.dtype)
+        if n_ws:
+            buffers["ws"] = torch.empty(n_ws, dtype=torch.uint8, device=device)
     d = buffers
     hout, hfin = d["hout"], d["hfin"]
     main = torch.cuda.current_stream(device)
@@ -146,9 +179,9 @@ def chunk_prefill_from_host(q, k, v, g, beta, scale=None, init_state=None, cu_se
             d["events"][s].record(cs)
     for s, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
         main.wait_event(d["events"][s])
-        _native.kda_chunk_prefill(d["q"][b0:b1], d["k"][b0:b1], d["v"][b0:b1], d["g"][b0:b1],
-                                  d["beta"][b0:b1], scale, d["state"], d["cu"][s, :N + 1],
-                                  d["out"][b0:b1], d["state"], main)
+        _native.kda_chunk_prefill_ws(d["q"][b0:b1], d["k"][b0:b1], d["v"][b0:b1], d["g"][b0:b1],
+                                     d["beta"][b0:b1], scale, d["state"], d["cu"][s, :N + 1],
+                                     d["out"][b0:b1], d["state"], d["ws"], main)
         ev = d["events"][segments + s]
         ev.record(main)
         bs.wait_event(ev)
