@@ -174,6 +174,31 @@ KDA_API int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
                                  void *stream);
 
 /*
+ * kda_chunk_prefill_ws without a caller workspace: the record ring lives in a
+ * file-scope device array of the library (48 clusters x 8 x 66,816 bytes = 25.7 MB per
+ * device, there from the moment the library is loaded).  The pages have no counterpart
+ * of this entry point; it exists for callers that cannot pass a workspace across the
+ * C ABI.
+ *
+ * Arguments, results and errors as for kda_chunk_prefill_ws, plus:
+ *   KDA_ERR_UNSUPPORTED  the device can keep more clusters resident than the array has
+ *                        room for (more than 48, i.e. more than 192 SMs).
+ * Every call on a device uses the SAME array: two calls whose executions overlap (on
+ * different streams, or from different host threads without ordering) race on it and
+ * give wrong results; calls enqueued on one stream are ordered and safe.  The array
+ * needs no initialisation.  The first call on each device looks up the array's
+ * address and queries the resident-cluster count, so make it before capturing the
+ * stream into a CUDA graph.
+ */
+KDA_API int kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
+                                      const float *g, const float *beta, float scale,
+                                      const float *init_state, const int32_t *cu_seqlens,
+                                      void *out, float *final_state,
+                                      int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
+                                      int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                                      int32_t out_dtype, void *stream);
+
+/*
  * Chunked prefill whose per-sequence states live in paged pool slots.
  *
  * The prompt path over the paged state group (vllm.cpp PR #122 "fold Kimi-Linear

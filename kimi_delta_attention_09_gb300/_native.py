@@ -23,6 +23,7 @@ ABI_VERSION = 2
 
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
             "kda_chunk_prefill", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_ws",
+            "kda_chunk_prefill_noalloc",
             "kda_chunk_prefill_paged", "kda_recurrent_decode")
 
 
@@ -53,6 +54,9 @@ def _load() -> ctypes.CDLL:
     lib.kda_chunk_prefill_ws.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
                                          i64, i32, i32, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]
     lib.kda_chunk_prefill_ws.restype = ctypes.c_int
+    lib.kda_chunk_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
+                                              i64, i32, i32, i32, i32, i32, i32, vp]
+    lib.kda_chunk_prefill_noalloc.restype = ctypes.c_int
     lib.kda_chunk_prefill_paged.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
                                             i64, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_chunk_prefill_paged.restype = ctypes.c_int
@@ -176,6 +180,36 @@ def kda_chunk_prefill_ws(q, k, v, g, beta, scale, init_state, cu_seqlens, out, f
                                   T, N, H, K, V, _dtype_code(q), _dtype_code(out), _ptr(workspace),
                                   ws_bytes, _stream_handle(stream))
     _check("kda_chunk_prefill_ws", rc)
+
+
+def kda_chunk_prefill_noalloc(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
+                              stream=None) -> None:
+    """Enqueue ``kda_chunk_prefill_noalloc``: ``kda_chunk_prefill_ws`` with the library's
+    own static device scratch (one call in flight per device at a time)."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out),
+                    ("cu_seqlens", cu_seqlens), ("init_state", init_state),
+                    ("final_state", final_state)):
+        if t is not None:
+            _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    _need(k.shape == q.shape and g.shape == q.shape, "q, k, g must be [T, H, K]")
+    _need(v.shape[:2] == (T, H) and out.shape == v.shape, "v, out must be [T, H, V]")
+    _need(beta.shape == (T, H), "beta must be [T, H]")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v must share one dtype")
+    import torch
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g, beta must be fp32")
+    _need(cu_seqlens.dtype == torch.int32, "cu_seqlens must be int32")
+    for s in (init_state, final_state):
+        if s is not None:
+            _need(s.dtype == torch.float32 and tuple(s.shape) == (N, H, K, V),
+                  "states must be fp32 [N, H, K, V]")
+    rc = lib.kda_chunk_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                       _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                       T, N, H, K, V, _dtype_code(q), _dtype_code(out),
+                                       _stream_handle(stream))
+    _check("kda_chunk_prefill_noalloc", rc)
 
 
 def kda_chunk_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens, out,

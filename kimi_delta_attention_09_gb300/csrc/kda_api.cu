@@ -2,6 +2,7 @@
 // alias guard and kernel selection.  No allocation, no synchronisation.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "kda.h"
 #include "kda_internal.cuh"
@@ -45,6 +46,37 @@ int launch_prefill(const kda::PrefillArgs &a, void *stream)
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return finish(kda::prefill_tc_supported(a) ? kda::launch_prefill_tc(a, st)
                                                : kda::launch_prefill_simt(a, st));
+}
+
+// Scratch of kda_chunk_prefill_noalloc: the cluster kernel's record ring for up to 48
+// clusters resident at once, in a file-scope device array (nothing is allocated; the
+// array exists once per device for the life of the loaded library).
+constexpr size_t kNoAllocClusters = 48;
+constexpr size_t kNoAllocScratchBytes = kNoAllocClusters * kda::kPrefillRrRing * kda::kPrefillRrRecordBytes;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the scratch on the current device, resolved once per device.
+void *noalloc_scratch()
+{
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        g_last_cuda_error = (int)(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) {
+            g_last_cuda_error = (int)e;
+            return nullptr;
+        }
+        addr[dev] = p;
+    }
+    return addr[dev];
 }
 
 // Validation shared by kda_chunk_prefill and kda_chunk_prefill_ws: fills `a` and the
@@ -165,6 +197,28 @@ int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
     for (const Range &r : ranges)
         if (overlaps(r_ws, r)) return KDA_ERR_ALIAS;
     return finish(kda::launch_prefill_rr(a, workspace, static_cast<cudaStream_t>(stream)));
+}
+
+int kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
+                              const float *g, const float *beta, float scale,
+                              const float *init_state, const int32_t *cu_seqlens,
+                              void *out, float *final_state,
+                              int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
+                              int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                              int32_t out_dtype, void *stream)
+{
+    kda::PrefillArgs a;
+    Range ranges[9];
+    const int st = check_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
+                                 total_tokens, num_seqs, num_heads, head_dim_k, head_dim_v, dtype,
+                                 out_dtype, a, ranges);
+    if (st != KDA_OK || num_seqs == 0) return st;
+    const size_t need = kda::prefill_rr_workspace_bytes(a);
+    if (need == 0) return launch_prefill(a, stream);   // shapes without the cluster kernel
+    if (need > kNoAllocScratchBytes) return KDA_ERR_UNSUPPORTED;
+    void *ws = noalloc_scratch();
+    if (!ws) return KDA_ERR_CUDA;
+    return finish(kda::launch_prefill_rr(a, ws, static_cast<cudaStream_t>(stream)));
 }
 
 int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,

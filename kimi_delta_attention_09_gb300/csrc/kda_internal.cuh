@@ -68,6 +68,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 // Chunked prefill on tensor cores with the per-chunk operands built once per head by a
 // 4-CTA cluster and shared through a caller workspace (same support as the above).
 size_t prefill_rr_workspace_bytes(const PrefillArgs &a);
+constexpr size_t kPrefillRrRecordBytes = 66816;   // one chunk's operand record
+constexpr int kPrefillRrRing = 8;                 // records per cluster
 cudaError_t launch_prefill_rr(const PrefillArgs &a, void *workspace, cudaStream_t stream);
 // One-token paged decode.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);

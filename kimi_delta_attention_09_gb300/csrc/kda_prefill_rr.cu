@@ -54,6 +54,7 @@ struct Rec {
     static constexpr int bytes = pm + KD * 4;
 };
 static_assert(Rec::bytes % 16 == 0, "bulk copies move multiples of 16 bytes");
+static_assert(Rec::bytes == kPrefillRrRecordBytes && kRing == kPrefillRrRing, "record ring size");
 
 // mbarriers
 struct Bar { enum { slot_full = 0, slot_free = 2, a = slot_free + kRing, s1 = a + 1, s3 = s1 + 1,
