@@ -41,6 +41,7 @@ constexpr int kBarBuild = 1;    // named barrier of the builder group
 constexpr int kBarStep = 2;     // named barrier of the state-step group
 constexpr int kRanks = kVTiles; // CTAs per cluster; rank j builds the chunks n = j (mod 4)
 constexpr int kRing = 8;        // records per cluster in the global ring
+constexpr int LDX = VT + 8;     // f16 row stride of beta X [64][32]: 80 B (conflict-free ldmatrix)
 
 // Operand record of one chunk: the byte image of the shared-memory tiles the state step
 // reads (SW128 tiles keep their swizzle at any 1024-byte aligned base).
@@ -65,7 +66,7 @@ struct Smem {
     static constexpr int slot_v = (Rec::bytes + 1023) / 1024 * 1024;   // v tile bf16 [64][32]
     static constexpr int slot_bytes = slot_v + C * VT * 2;            // record + v tile
     static constexpr int ht = 2 * slot_bytes;                // SW128 (2^m h)^T f16 32 x 128
-    static constexpr int xt = ht;                            // f16 (beta X)^T [32][LD64] once S1 is done
+    static constexpr int xs = ht;                            // f16 beta X [64][LDX] once S1 is done
     static constexpr int dt = ht + VT * KD * 2;              // SW128 D^T f16 32 x 64
     static constexpr int st_aop = dt + VT * C * 2;           // builder: SW128 [a_k; a_q]
     static constexpr int st_bk = st_aop + 2 * C * KD * 2;    // builder: SW128 b 64 x 128
@@ -86,7 +87,7 @@ static_assert(Smem::slot_bytes % 1024 == 0 && Smem::ht % 1024 == 0 && Smem::dt %
               Smem::st_aop % 1024 == 0 && Smem::st_bk % 1024 == 0 && Smem::st_tw % 1024 == 0 &&
               Smem::st_akk % 1024 == 0, "SW128 tiles need 1024-byte alignment");
 static_assert(C * LD64 * 2 <= C * KD * 2 && Smem::first + KD * 4 <= Smem::st_tw, "b-space aliases");
-static_assert(VT * LD64 * 2 <= VT * KD * 2, "(beta X)^T fits in the h^T space");
+static_assert(C * LDX * 2 <= VT * KD * 2, "beta X fits in the h^T space");
 
 struct RrMaps {
     CUtensorMap q, k, g;   // box 128 channels x 1 head x 64 tokens (L2 prefetch of a builder's next chunk)
@@ -500,7 +501,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
         const int hc = (warp >> 2) & 1;
         __half *ht = reinterpret_cast<__half *>(sm + Smem::ht);
         __half *dt = reinterpret_cast<__half *>(sm + Smem::dt);
-        __half *xt = reinterpret_cast<__half *>(sm + Smem::xt);
+        __half *xs = reinterpret_cast<__half *>(sm + Smem::xs);
         Tout *out = static_cast<Tout *>(a.out);
 
         // arm slot lci % 2 for chunk lci: expected bytes, the v tile, and the arrival on
@@ -603,6 +604,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                     for (int v = 0; v < 16; ++v) xv[v] += xb[v];
                     const float b = bts[r];
                     const uint4 *vrow = reinterpret_cast<const uint4 *>(vsl + r * VT + 16 * half);
+                    uint32_t xw[8];
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const uint4 wv = vrow[j];
@@ -611,40 +613,49 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                         for (int u = 0; u < 4; ++u) {
                             const float2 vv = __bfloat1622float2(p2[u]);
                             const int v = 8 * j + 2 * u;
-                            xt[(16 * half + v) * LD64 + r] = __float2half_rn(b * (vv.x - xv[v]));
-                            xt[(16 * half + v + 1) * LD64 + r] = __float2half_rn(b * (vv.y - xv[v + 1]));
+                            xw[4 * j + u] = pack_h2(b * (vv.x - xv[v]), b * (vv.y - xv[v + 1]));
                         }
                     }
+                    uint4 *xrow = reinterpret_cast<uint4 *>(xs + r * LDX + 16 * half);
+                    xrow[0] = make_uint4(xw[0], xw[1], xw[2], xw[3]);
+                    xrow[1] = make_uint4(xw[4], xw[5], xw[6], xw[7]);
                     tc_fence_before();
                 }
-                named_bar_sync(kBarStep, kGroup);   // S1 is complete: ht (= xt) and D1 rows are free
+                named_bar_sync(kBarStep, kGroup);   // S1 is complete: ht (= xs) and D1 rows are free
 
-                // ---------------- S2: D^T = (beta X)^T T^T  (mma.sync; T lower triangular: k-blocks <= qw/2)
+                // ---------------- S2: D = T (beta X) on mma.sync, warp w: rows [16 (w % 4), +16),
+                //                  value columns [16 (w / 4), +16); T lower triangular: k-blocks
+                //                  <= the row block.  D^T goes to dt (SW128) by stmatrix.
                 {
-                    const int mt = warp & 1;
+                    const int mt = warp & 3, nh = warp >> 2;
+                    float dk[4][2][4];   // one accumulator pair per k-block (no chained mma)
+                    const int arow = 16 * mt + (lane & 15), akoff = (lane >> 4) << 3;
+                    const int xrow = (lane & 7) + (((lane >> 3) & 1) << 3), xcol = 16 * nh + ((lane >> 4) << 3);
 #pragma unroll
-                    for (int jq = 0; jq < 2; ++jq) {
-                        const int qw = (warp >> 1) + 4 * jq, rblk = qw >> 1;
-                        float dk[4][4];   // one accumulator per k-block (no chained mma)
-                        const int trow = 8 * qw + (lane & 7), tk = ((lane >> 3) & 1) << 3;
+                    for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            dk[ks][0] = dk[ks][1] = dk[ks][2] = dk[ks][3] = 0.f;
-                            if (ks <= rblk) {
-                                uint32_t af[4], bt[2];
-                                ldsm_x4(smem_u32(xt + a_off(lane, 16 * mt, 16 * ks, LD64)), af[0], af[1], af[2], af[3]);
-                                ldsm_x2(smem_u32(ta + sw128(trow, 16 * ks + tk, 2 * C)), bt[0], bt[1]);
-                                mma16816(dk[ks], af, bt[0], bt[1]);
-                            }
+                        for (int nt = 0; nt < 2; ++nt) dk[ks][nt][0] = dk[ks][nt][1] = dk[ks][nt][2] = dk[ks][nt][3] = 0.f;
+                        if (ks <= mt) {
+                            uint32_t af[4], bf[4];
+                            ldsm_x4(smem_u32(ta + sw128(arow, 16 * ks + akoff, 2 * C)), af[0], af[1], af[2], af[3]);
+                            ldsm_x4_t(smem_u32(xs + (16 * ks + xrow) * LDX + xcol), bf[0], bf[1], bf[2], bf[3]);
+                            mma16816(dk[ks][0], af, bf[0], bf[1]);
+                            mma16816(dk[ks][1], af, bf[2], bf[3]);
                         }
-                        float dacc[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) dacc[e] = (dk[0][e] + dk[1][e]) + (dk[2][e] + dk[3][e]);
-                        const int r = 8 * qw + 2 * tig;
-                        const int v0 = 16 * mt + g8;
-                        *reinterpret_cast<uint32_t *>(dt + sw128(v0, r, VT)) = pack_h2(dacc[0], dacc[1]);
-                        *reinterpret_cast<uint32_t *>(dt + sw128(v0 + 8, r, VT)) = pack_h2(dacc[2], dacc[3]);
                     }
+                    uint32_t dw[4];   // stmatrix order: (nt 0, rows g), (nt 0, rows g + 8), (nt 1, g), (nt 1, g + 8)
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        float e[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            e[q] = (dk[0][nt][q] + dk[1][nt][q]) + (dk[2][nt][q] + dk[3][nt][q]);
+                        dw[2 * nt] = pack_h2(e[0], e[1]);
+                        dw[2 * nt + 1] = pack_h2(e[2], e[3]);
+                    }
+                    const int mi = lane >> 3, mj = lane & 7;
+                    stsm_x4_t(smem_u32(dt + sw128(16 * nh + 8 * (mi >> 1) + mj, 16 * mt + 8 * (mi & 1), VT)),
+                              dw[0], dw[1], dw[2], dw[3]);
                 }
                 fence_proxy_async_smem();
                 named_bar_sync(kBarStep, kGroup);
@@ -668,6 +679,9 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                 }
                 if (!mbar_wait(bar(Bar::s3), par)) failed = true;
                 tc_fence_after();
+                // every read of slot s is done (the generic ones before the barrier above, the
+                // tcgen05 ones at the S3 commit): arm it for chunk ci + 2 while the output is stored
+                if (tid == 0 && lhave) arm_slot();
                 if (warp & 2) {   // rows 64..127 of D1: o (warps 2, 3, 6, 7)
                     const int r = 32 * (warp & 1) + lane, half = warp >> 2;
                     float ov[16], ob[16];
@@ -678,9 +692,8 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                     if (r < len) store_row16(out + ((t0 + r) * H + h) * VD + vt * VT + 16 * half, ov, a.scale);
                 }
                 tc_fence_before();
-                // slot s and the step buffers are consumed: load chunk ci + 2 into slot s
+                // the step buffers are consumed
                 if (bar_red_or(kBarStep, kGroup, failed)) { failed = gfail = true; break; }
-                if (tid == 0 && lhave) arm_slot();
             }
             if (fin) {   // final state; error marker: NaN state
                 tc_fence_after();
