@@ -91,7 +91,9 @@ static_assert(C * LDX * 2 <= VT * KD * 2, "beta X fits in the h^T space");
 
 struct RrMaps {
     CUtensorMap q, k, g;   // box 128 channels x 1 head x 64 tokens (L2 prefetch of a builder's next chunk)
+    CUtensorMap beta;      // [T, H] fp32, box 4 heads x 64 tokens (L2 prefetch; H % 4 == 0 only)
     CUtensorMap v;         // box 32 columns x 1 head x 64 tokens
+    int beta_map;          // 0: no beta prefetch
 };
 
 // ------------------------------------------------------------------ cluster helpers
@@ -123,6 +125,11 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, i
 {
     asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n"
                  :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z) : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];\n"
+                 :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y) : "memory");
 }
 
 // bounded wait (acquire, cluster scope) for a phase completed by remote arrivals
@@ -231,7 +238,6 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
 {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g8 = lane >> 2, tig = lane & 3;
     const int rank = (int)cluster_ctarank();   // = value tile
     const int vt = rank;
     const int64_t cid = blockIdx.x / kRanks;
@@ -241,9 +247,10 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
     auto slot = [&](int s) { return sm + s * Smem::slot_bytes; };
     auto record = [&](int64_t ci) { return ws + ((int64_t)cid * kRing + (ci % kRing)) * Rec::bytes; };
 
-    // ---- tensor memory (256 columns: [0, 32) and [32, 64) the step accumulator D1 in
-    //      two K halves (issued by two threads), [64, 96) the state h^T with lane = key
-    //      channel, column = value, [128, 192) the A matrices)
+    // ---- tensor memory (256 columns: per chunk parity p, [64 p, 64 p + 32) and
+    //      [64 p + 32, 64 p + 64) the step accumulator D1 in two K halves (issued by two
+    //      threads; the output rows of chunk n are read during chunk n + 1), [128, 160)
+    //      the state h^T with lane = key channel, column = value, [192, 256) the A matrices)
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
                      :: "r"(smem_u32(sm + Smem::tmem)), "r"(256) : "memory");
@@ -260,7 +267,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
     cluster_sync_all();   // every CTA's barriers exist before any remote arrival
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sm + Smem::tmem);
-    const uint32_t tD1 = tmem, tD1b = tmem + 32, tH = tmem + 64, tDA = tmem + 128;
+    const uint32_t tH = tmem + 128, tDA = tmem + 192;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;   // TMEM lane quadrant of this warp
     bool failed = false;
 
@@ -296,6 +303,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                 tma_prefetch_3d(&maps.q, 0, hh, z);
                 tma_prefetch_3d(&maps.k, 0, hh, z);
                 tma_prefetch_3d(&maps.g, 0, hh, z);
+                if (maps.beta_map) tma_prefetch_2d(&maps.beta, hh & ~3, z);
             }
         };
         Cursor pc;
@@ -321,13 +329,16 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
 
             // ---------------- P1: gate cumsum in exp2 space; thread = (channel pair, 16-row group E)
             const int pcp = gtid & 63, pE = gtid >> 6, pc0 = 2 * pcp;
-            // this thread's 16 rows of g (channels pc0, pc0 + 1), all loads in flight at once
+            // this thread's 16 rows of g, k and q (channels pc0, pc0 + 1): all loads in flight at once
             float2 gx[16];
+            uint32_t kq[16], qq[16];   // bf16 pairs
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int r = 16 * pE + u;
-                gx[u] = r < len ? __ldg(reinterpret_cast<const float2 *>(gin + ((t0 + r) * H + h) * KD + pc0))
-                                : make_float2(0.f, 0.f);
+                const int64_t off = ((t0 + r) * H + h) * KD + pc0;
+                gx[u] = r < len ? __ldg(reinterpret_cast<const float2 *>(gin + off)) : make_float2(0.f, 0.f);
+                kq[u] = r < len ? __ldg(reinterpret_cast<const unsigned int *>(kin + off)) : 0u;
+                qq[u] = r < len ? __ldg(reinterpret_cast<const unsigned int *>(qin + off)) : 0u;
             }
 #pragma unroll
             for (int u = 0; u < 16; ++u) gx[u] = make_float2(gx[u].x * kLog2e, gx[u].y * kLog2e);
@@ -361,14 +372,6 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
             float amax = 0.f;
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
-                uint32_t kq[8], qq[8];   // bf16 pairs of these eight rows, loads in flight at once
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int r = 16 * pE + 8 * hb + u;
-                    const int64_t off = ((t0 + r) * H + h) * KD + pc0;
-                    kq[u] = r < len ? __ldg(reinterpret_cast<const unsigned int *>(kin + off)) : 0u;
-                    qq[u] = r < len ? __ldg(reinterpret_cast<const unsigned int *>(qin + off)) : 0u;
-                }
                 float khx[8], khy[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
@@ -377,8 +380,8 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                     amax = fmaxf(amax, fmaxf(fabsf(xx), fabsf(xy)));
                     const float ex = exp2f(xx), ey = exp2f(xy);
                     const float ix = rcp_approx(ex), iy = rcp_approx(ey);
-                    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kq[u]));
-                    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq[u]));
+                    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kq[8 * hb + u]));
+                    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq[8 * hb + u]));
                     *reinterpret_cast<uint32_t *>(aop + sw128(r, pc0, 2 * C)) = pack_h2(kv.x * ex, kv.y * ey);
                     *reinterpret_cast<uint32_t *>(aop + sw128(C + r, pc0, 2 * C)) = pack_h2(qv.x * ex, qv.y * ey);
                     const float b0 = kv.x * ix, b1 = kv.y * iy;
@@ -504,26 +507,50 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
         __half *xs = reinterpret_cast<__half *>(sm + Smem::xs);
         Tout *out = static_cast<Tout *>(a.out);
 
-        // arm slot lci % 2 for chunk lci: expected bytes, the v tile, and the arrival on
-        // the slot_free barrier of the chunk's builder (run by thread 0 once the slot's
-        // previous chunk is consumed)
+        // Arming slot lci % 2 for chunk lci (thread kArmer): the local part -- expected
+        // bytes and the TMA of this CTA's v tile -- once the slot's v region is free, then
+        // the arrival on the chunk's builder's slot_free barrier once every read of the
+        // slot is done (the builder's multicast overwrites it).
+        constexpr int kArmer = 64;   // warp 2: idle while S3 runs
         Cursor lc{0, 0, 0, 0};
         int64_t lci = 0;
         bool lhave = false;
-        auto arm_slot = [&]() {
+        auto arm_local = [&]() {
             const int s = (int)(lci & 1);
             fence_proxy_async_smem();     // earlier generic reads of the slot come first
             const uint32_t mb = bar(Bar::slot_full + s);
             mbar_arrive_expect_tx(mb, Rec::bytes + C * VT * 2);
             tma_load_3d(smem_u32(slot(s) + Smem::slot_v), &maps.v, vt * VT, (int)(lc.w % H), (int)lc.t0, mb);
+        };
+        auto arm_remote = [&]() {
             mbar_arrive_remote_relaxed(bar(Bar::slot_free + (int)(lci % kRing)), (uint32_t)(lci % kRanks));
             ++lci;
             lhave = cursor_next(lc, a, G);
         };
-        if (tid == 0) {
+        if (tid == kArmer) {
             lhave = cursor_seek(lc, a, cid, G);
-            for (int i = 0; i < 2 && lhave; ++i) arm_slot();
+            for (int i = 0; i < 2 && lhave; ++i) { arm_local(); arm_remote(); }
         }
+        // output rows of the previous chunk (warps 2, 3, 6, 7), stored during the next
+        // chunk's S1 / X phase, when those warps are otherwise idle
+        bool pend = false;
+        int pend_par = 0, pend_len = 0, pend_h = 0;
+        int64_t pend_t0 = 0;
+        auto flush_o = [&]() {
+            if (!pend) return;
+            tc_fence_after();
+            const int r = 32 * (warp & 1) + lane, half = warp >> 2;
+            const uint32_t d1 = tmem + 64 * pend_par;
+            float ov[16], ob[16];
+            tmem_ld16(d1 + lane_off + 16 * half, ov);
+            tmem_ld16(d1 + 32 + lane_off + 16 * half, ob);
+#pragma unroll
+            for (int v = 0; v < 16; ++v) ov[v] += ob[v];
+            if (r < pend_len)
+                store_row16(out + ((pend_t0 + r) * H + pend_h) * VD + vt * VT + 16 * half, ov, a.scale);
+            tc_fence_before();
+            pend = false;
+        };
 
         int64_t ci = 0;
         bool gfail = false;   // group-uniform: set only from barrier reductions
@@ -556,6 +583,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                 if (bar_red_or(kBarStep, kGroup, failed)) { failed = gfail = true; break; }
                 if (tid == 0) *reinterpret_cast<volatile int64_t *>(sm + Smem::consumed) = ci + 1;
                 tc_fence_after();
+                const uint32_t tD1 = tmem + 64 * s, tD1b = tD1 + 32;   // this chunk's accumulators
                 const __half *aop = reinterpret_cast<const __half *>(sl + Rec::aop);
                 const __half *kht = reinterpret_cast<const __half *>(sl + Rec::kht);
                 const __half *ta = reinterpret_cast<const __half *>(sl + Rec::ta);
@@ -620,6 +648,8 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                     xrow[0] = make_uint4(xw[0], xw[1], xw[2], xw[3]);
                     xrow[1] = make_uint4(xw[4], xw[5], xw[6], xw[7]);
                     tc_fence_before();
+                } else {
+                    flush_o();   // the previous chunk's output rows
                 }
                 named_bar_sync(kBarStep, kGroup);   // S1 is complete: ht (= xs) and D1 rows are free
 
@@ -677,23 +707,23 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                                  kIdescM128N32, 1u);
                     umma_commit(bar(Bar::s3));
                 }
+                // slot s's v region is free (X is done): the local part of arming it for
+                // chunk ci + 2 runs while S3 does
+                const bool arming = tid == kArmer && lhave;
+                if (arming) arm_local();
                 if (!mbar_wait(bar(Bar::s3), par)) failed = true;
                 tc_fence_after();
-                // every read of slot s is done (the generic ones before the barrier above, the
-                // tcgen05 ones at the S3 commit): arm it for chunk ci + 2 while the output is stored
-                if (tid == 0 && lhave) arm_slot();
-                if (warp & 2) {   // rows 64..127 of D1: o (warps 2, 3, 6, 7)
-                    const int r = 32 * (warp & 1) + lane, half = warp >> 2;
-                    float ov[16], ob[16];
-                    tmem_ld16(tD1 + lane_off + 16 * half, ov);
-                    tmem_ld16(tD1b + lane_off + 16 * half, ob);
-#pragma unroll
-                    for (int v = 0; v < 16; ++v) ov[v] += ob[v];
-                    if (r < len) store_row16(out + ((t0 + r) * H + h) * VD + vt * VT + 16 * half, ov, a.scale);
+                // every read of slot s is done (generic ones before the barrier above, tcgen05
+                // ones at the S3 commit): the builder may overwrite it
+                if (arming) arm_remote();
+                if (warp & 2) {   // rows 64..127 of D1 (the output) are stored during the next chunk
+                    pend = true;
+                    pend_par = s;
+                    pend_t0 = t0;
+                    pend_len = len;
+                    pend_h = h;
                 }
                 tc_fence_before();
-                // the step buffers are consumed
-                if (bar_red_or(kBarStep, kGroup, failed)) { failed = gfail = true; break; }
             }
             if (fin) {   // final state; error marker: NaN state
                 tc_fence_after();
@@ -710,8 +740,9 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
             tc_fence_before();
             named_bar_sync(kBarStep, kGroup);   // TMEM h is read before the next item's init
         }
+        if (warp & 2) flush_o();   // the last chunk's output rows
         if (failed) {   // copies and MMAs still in flight get one more bounded wait
-            if (tid == 0)
+            if (tid == kArmer)
                 for (int64_t c = ci; c < lci; ++c) mbar_wait(bar(Bar::slot_full + (int)(c & 1)), (uint32_t)((c >> 1) & 1));
             mbar_wait(bar(Bar::s1), (uint32_t)(ci & 1));
             mbar_wait(bar(Bar::s3), (uint32_t)(ci & 1));
@@ -772,6 +803,7 @@ cudaError_t launch_rr_t(const PrefillArgs &a, void *ws, cudaStream_t stream)
             !encode_map(&maps.g, a.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T, H, KD, KD) ||
             !encode_map(&maps.v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, VD, VT))
             return cudaErrorInvalidValue;
+        maps.beta_map = (H % 4 == 0) && encode_map_2d(&maps.beta, a.beta, T, H);
     }
     cudaError_t e = cudaFuncSetAttribute(kda_prefill_rr_kernel<Tout>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::total);
