@@ -170,3 +170,68 @@ def test_binding_refuses_missing_library(tmp_path, monkeypatch):
                         lambda p, _e=os.path.exists: False if p.endswith("libkda.so") else _e(p))
     with pytest.raises(RuntimeError, match="not built"):
         spec.loader.exec_module(mod)
+
+
+def _prefill_ws(native, ws, ws_bytes, **kw):
+    """kda_chunk_prefill_ws with the argument set of _prefill (K = V = 128, bf16 by
+    default: the shapes that need a workspace)."""
+    a = dict(q=BASE, k=BASE + (1 << 24), v=BASE + (2 << 24), g=BASE + (3 << 24),
+             beta=BASE + (4 << 24), scale=0.125, init=BASE + (5 << 24), cu=BASE + (6 << 24),
+             out=BASE + (7 << 24), final=BASE + (8 << 24), T=100, N=2, H=2, K=128, V=128,
+             dtype=1, out_dtype=1)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return native.lib.kda_chunk_prefill_ws(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
+        vp(a["init"]), vp(a["cu"]), vp(a["out"]), vp(a["final"]), a["T"], a["N"], a["H"],
+        a["K"], a["V"], a["dtype"], a["out_dtype"], vp(ws), ws_bytes, None)
+
+
+def test_workspace_query_is_zero_without_the_cluster_kernel(native):
+    q = native.lib.kda_chunk_prefill_workspace_bytes
+    assert q(2, 2, 128, 128, 0) == 0      # fp32 inputs
+    assert q(2, 2, 64, 128, 1) == 0       # K = 64
+    assert q(2, 2, 128, 64, 1) == 0       # V = 64
+    assert q(0, 2, 128, 128, 1) == 0      # no sequences
+    n = q(2, 2, 128, 128, 1)
+    assert n > 0 and n % 66816 == 0       # whole records of the ring
+
+
+def test_prefill_ws_validation_and_alias(native):
+    need = native.lib.kda_chunk_prefill_workspace_bytes(2, 2, 128, 128, 1)
+    ws = BASE + (1 << 36)
+    # the shared argument checks come first
+    assert _prefill_ws(native, ws, need, q=None) == native.KDA_ERR_INVALID_ARG
+    assert _prefill_ws(native, ws, need, K=96) == native.KDA_ERR_UNSUPPORTED
+    assert _prefill_ws(native, ws, need, out=BASE) == native.KDA_ERR_ALIAS
+    assert _prefill_ws(native, None, 0, N=0) == native.KDA_OK
+    # the workspace itself: missing, too small, misaligned
+    assert _prefill_ws(native, None, 0) == native.KDA_ERR_INVALID_ARG
+    assert _prefill_ws(native, ws, need - 16) == native.KDA_ERR_INVALID_ARG
+    assert _prefill_ws(native, ws + 8, need) == native.KDA_ERR_INVALID_ARG
+    # ... and overlapping any input or output (partially, at either end)
+    assert _prefill_ws(native, BASE + (1 << 24) - need + 16, need) == native.KDA_ERR_ALIAS   # k
+    assert _prefill_ws(native, BASE + (7 << 24) + 4096, need) == native.KDA_ERR_ALIAS       # out
+    assert _prefill_ws(native, BASE + (8 << 24) - 16, need) == native.KDA_ERR_ALIAS         # final
+    assert _prefill_ws(native, BASE + (6 << 24), need) == native.KDA_ERR_ALIAS              # cu_seqlens
+
+
+def test_prefill_noalloc_validation(native):
+    vp = ctypes.c_void_p
+
+    def call(**kw):
+        a = dict(q=BASE, k=BASE + (1 << 24), v=BASE + (2 << 24), g=BASE + (3 << 24),
+                 beta=BASE + (4 << 24), scale=0.125, init=BASE + (5 << 24), cu=BASE + (6 << 24),
+                 out=BASE + (7 << 24), final=BASE + (8 << 24), T=100, N=2, H=2, K=128, V=128,
+                 dtype=1, out_dtype=1)
+        a.update(kw)
+        return native.lib.kda_chunk_prefill_noalloc(
+            vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
+            vp(a["init"]), vp(a["cu"]), vp(a["out"]), vp(a["final"]), a["T"], a["N"], a["H"],
+            a["K"], a["V"], a["dtype"], a["out_dtype"], None)
+
+    assert call(q=None) == native.KDA_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == native.KDA_ERR_INVALID_ARG
+    assert call(V=96) == native.KDA_ERR_UNSUPPORTED
+    assert call(final=BASE + (1 << 24)) == native.KDA_ERR_ALIAS
+    assert call(N=0) == native.KDA_OK
