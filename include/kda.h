@@ -22,7 +22,8 @@
  *                            operands instead of each building them (faster; same
  *                            result up to fp32 rounding).
  *   kda_chunk_prefill_paged -- the same prefill with the initial and final states in
- *                            paged pool slots selected per sequence (in place).
+ *                            paged pool slots selected per sequence (in place); its _ws
+ *                            form runs on the shared-operand kernel.
  *   kda_recurrent_decode  -- one token per sequence against the state held in a
  *                            paged pool slot, updated in place (state slots keyed
  *                            by per-sequence indices, PR #122 block B2).
@@ -224,6 +225,21 @@ KDA_API int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
                                     int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
                                     int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
                                     int32_t dtype, int32_t out_dtype, void *stream);
+
+/*
+ * kda_chunk_prefill_paged with a caller workspace: the same operation on the
+ * shared-operand cluster kernel of kda_chunk_prefill_ws (same workspace rules and size,
+ * kda_chunk_prefill_workspace_bytes(num_seqs, ...)).  The workspace must not overlap
+ * any other argument, the pool included (KDA_ERR_ALIAS).
+ */
+KDA_API int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void *v,
+                                       const float *g, const float *beta, float scale,
+                                       float *state_pool, const int32_t *state_idx,
+                                       const int32_t *cu_seqlens, void *out,
+                                       int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
+                                       int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+                                       int32_t dtype, int32_t out_dtype, void *workspace,
+                                       size_t workspace_bytes, void *stream);
 
 /*
  * One recurrent decode step for num_seqs sequences with paged states.

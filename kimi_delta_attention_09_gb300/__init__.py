@@ -11,12 +11,14 @@ from __future__ import annotations
 
 __all__ = ["chunk_prefill", "chunk_prefill_paged", "chunk_prefill_from_host", "recurrent_decode",
            "prefill_workspace", "kda_chunk_prefill", "kda_chunk_prefill_ws",
+           "kda_chunk_prefill_paged_ws", "kda_chunk_prefill_noalloc",
            "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_paged", "kda_recurrent_decode"]
 
 
 def __getattr__(name):
     if name in ("kda_chunk_prefill", "kda_chunk_prefill_ws", "kda_chunk_prefill_workspace_bytes",
-                "kda_chunk_prefill_paged", "kda_recurrent_decode", "KdaError"):
+                "kda_chunk_prefill_paged", "kda_chunk_prefill_paged_ws", "kda_chunk_prefill_noalloc",
+                "kda_recurrent_decode", "KdaError"):
         from . import _native
         return getattr(_native, name)
     raise AttributeError(name)
@@ -76,9 +78,11 @@ def chunk_prefill(q, k, v, g, beta, scale=None, init_state=None, cu_seqlens=None
 
 
 def chunk_prefill_paged(q, k, v, g, beta, state_pool, state_idx, scale=None, cu_seqlens=None,
-                        out_dtype=None, stream=None):
+                        out_dtype=None, stream=None, workspace=None):
     """Chunked prefill with each sequence's state in slot ``state_idx[n]`` of
-    ``state_pool`` (read as the initial state, overwritten with the final state)."""
+    ``state_pool`` (read as the initial state, overwritten with the final state).  Runs
+    ``kda_chunk_prefill_paged_ws`` with ``workspace`` or the cached one of
+    ``prefill_workspace``."""
     import torch
     from . import _native
     T, H, K = q.shape
@@ -87,8 +91,11 @@ def chunk_prefill_paged(q, k, v, g, beta, state_pool, state_idx, scale=None, cu_
     if cu_seqlens is None:
         cu_seqlens = torch.tensor([0, T], dtype=torch.int32, device=q.device)
     out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
-    _native.kda_chunk_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens,
-                                    out, stream)
+    if workspace is None:
+        workspace = prefill_workspace(cu_seqlens.numel() - 1, H, K, v.shape[-1], q.dtype,
+                                      q.device, stream)
+    _native.kda_chunk_prefill_paged_ws(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens,
+                                       out, workspace, stream)
     return out
 
 

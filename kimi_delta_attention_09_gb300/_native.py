@@ -23,7 +23,7 @@ ABI_VERSION = 2
 
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
             "kda_chunk_prefill", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_ws",
-            "kda_chunk_prefill_noalloc",
+            "kda_chunk_prefill_noalloc", "kda_chunk_prefill_paged_ws",
             "kda_chunk_prefill_paged", "kda_recurrent_decode")
 
 
@@ -60,6 +60,10 @@ def _load() -> ctypes.CDLL:
     lib.kda_chunk_prefill_paged.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
                                             i64, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_chunk_prefill_paged.restype = ctypes.c_int
+    lib.kda_chunk_prefill_paged_ws.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
+                                               i64, i32, i32, i32, i32, i32, i32, i32, vp,
+                                               ctypes.c_size_t, vp]
+    lib.kda_chunk_prefill_paged_ws.restype = ctypes.c_int
     lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp,
                                          i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_recurrent_decode.restype = ctypes.c_int
@@ -239,6 +243,37 @@ def kda_chunk_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_s
                                      _ptr(out), T, N, S, H, K, V, _dtype_code(q), _dtype_code(out),
                                      _stream_handle(stream))
     _check("kda_chunk_prefill_paged", rc)
+
+
+def kda_chunk_prefill_paged_ws(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens, out,
+                               workspace, stream=None) -> None:
+    """Enqueue ``kda_chunk_prefill_paged_ws``: ``kda_chunk_prefill_paged`` plus ``workspace``
+    (as for ``kda_chunk_prefill_ws``)."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    S = state_pool.shape[0]
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out),
+                    ("cu_seqlens", cu_seqlens), ("state_pool", state_pool),
+                    ("state_idx", state_idx), ("workspace", workspace)):
+        if t is not None:
+            _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    import torch
+    _need(k.shape == q.shape and g.shape == q.shape, "q, k, g must be [T, H, K]")
+    _need(v.shape[:2] == (T, H) and out.shape == v.shape, "v, out must be [T, H, V]")
+    _need(beta.shape == (T, H), "beta must be [T, H]")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v must share one dtype")
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g, beta must be fp32")
+    _need(cu_seqlens.dtype == torch.int32, "cu_seqlens must be int32")
+    _need(tuple(state_pool.shape[1:]) == (H, K, V) and state_pool.dtype == torch.float32,
+          "state_pool must be fp32 [S, H, K, V]")
+    _need(state_idx.dtype == torch.int32 and state_idx.numel() == N, "state_idx must be int32 [N]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib.kda_chunk_prefill_paged_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                        _ptr(state_pool), _ptr(state_idx), _ptr(cu_seqlens),
+                                        _ptr(out), T, N, S, H, K, V, _dtype_code(q), _dtype_code(out),
+                                        _ptr(workspace), ws_bytes, _stream_handle(stream))
+    _check("kda_chunk_prefill_paged_ws", rc)
 
 
 def kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out,

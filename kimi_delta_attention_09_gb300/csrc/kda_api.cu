@@ -129,6 +129,56 @@ int check_prefill(const void *q, const void *k, const void *v, const float *g, c
     return KDA_OK;
 }
 
+// Validation of the paged prefill entry points: fills `a` and the byte ranges of every
+// input and of out and the pool (for the workspace alias check).
+int check_prefill_paged(const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, float scale, float *state_pool,
+                        const int32_t *state_idx, const int32_t *cu_seqlens, void *out,
+                        int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
+                        int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                        int32_t out_dtype, kda::PrefillArgs &a, Range (&ranges)[9])
+{
+    if (total_tokens < 0 || num_seqs < 0 || num_slots < 0 || num_heads < 1 ||
+        !std::isfinite(scale))
+        return KDA_ERR_INVALID_ARG;
+    if (!dtype_supported(dtype) || !dtype_supported(out_dtype)) return KDA_ERR_UNSUPPORTED;
+    if (!dims_supported(head_dim_k) || !dims_supported(head_dim_v)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KDA_OK;
+    if (!cu_seqlens || !aligned16(cu_seqlens) || !state_idx || !aligned16(state_idx))
+        return KDA_ERR_INVALID_ARG;
+    if (num_slots > 0 && (!state_pool || !aligned16(state_pool))) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0) {
+        const void *req[] = {q, k, v, g, beta, out};
+        for (const void *p : req)
+            if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
+    }
+    const uint64_t T = (uint64_t)total_tokens, H = (uint64_t)num_heads;
+    const uint64_t K = (uint64_t)head_dim_k, V = (uint64_t)head_dim_v;
+    const uint64_t es = dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const uint64_t eo = out_dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const Range in[] = {{q, T * H * K * es}, {k, T * H * K * es}, {v, T * H * V * es},
+                        {g, T * H * K * 4}, {beta, T * H * 4},
+                        {cu_seqlens, ((uint64_t)num_seqs + 1) * 4},
+                        {state_idx, (uint64_t)num_seqs * 4}};
+    const Range r_out{out, T * H * V * eo};
+    const Range r_pool{state_pool, (uint64_t)num_slots * H * K * V * 4};
+    for (const Range &r : in)
+        if (overlaps(r_out, r) || overlaps(r_pool, r)) return KDA_ERR_ALIAS;
+    if (overlaps(r_out, r_pool)) return KDA_ERR_ALIAS;
+    for (int i = 0; i < 7; ++i) ranges[i] = in[i];
+    ranges[7] = r_out;
+    ranges[8] = r_pool;
+
+    a = kda::PrefillArgs{};
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
+    a.cu_seqlens = cu_seqlens; a.out = out;
+    a.state_pool = state_pool; a.state_idx = state_idx; a.num_slots = num_slots;
+    a.total_tokens = total_tokens; a.num_seqs = num_seqs;
+    a.num_heads = num_heads; a.head_dim_k = head_dim_k; a.head_dim_v = head_dim_v;
+    a.dtype = dtype; a.out_dtype = out_dtype;
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,42 +279,37 @@ int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
                             int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
                             int32_t dtype, int32_t out_dtype, void *stream)
 {
-    if (total_tokens < 0 || num_seqs < 0 || num_slots < 0 || num_heads < 1 ||
-        !std::isfinite(scale))
-        return KDA_ERR_INVALID_ARG;
-    if (!dtype_supported(dtype) || !dtype_supported(out_dtype)) return KDA_ERR_UNSUPPORTED;
-    if (!dims_supported(head_dim_k) || !dims_supported(head_dim_v)) return KDA_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return KDA_OK;
-    if (!cu_seqlens || !aligned16(cu_seqlens) || !state_idx || !aligned16(state_idx))
-        return KDA_ERR_INVALID_ARG;
-    if (num_slots > 0 && (!state_pool || !aligned16(state_pool))) return KDA_ERR_INVALID_ARG;
-    if (total_tokens > 0) {
-        const void *req[] = {q, k, v, g, beta, out};
-        for (const void *p : req)
-            if (!p || !aligned16(p)) return KDA_ERR_INVALID_ARG;
-    }
-    const uint64_t T = (uint64_t)total_tokens, H = (uint64_t)num_heads;
-    const uint64_t K = (uint64_t)head_dim_k, V = (uint64_t)head_dim_v;
-    const uint64_t es = dtype == KDA_DTYPE_BF16 ? 2 : 4;
-    const uint64_t eo = out_dtype == KDA_DTYPE_BF16 ? 2 : 4;
-    const Range in[] = {{q, T * H * K * es}, {k, T * H * K * es}, {v, T * H * V * es},
-                        {g, T * H * K * 4}, {beta, T * H * 4},
-                        {cu_seqlens, ((uint64_t)num_seqs + 1) * 4},
-                        {state_idx, (uint64_t)num_seqs * 4}};
-    const Range r_out{out, T * H * V * eo};
-    const Range r_pool{state_pool, (uint64_t)num_slots * H * K * V * 4};
-    for (const Range &r : in)
-        if (overlaps(r_out, r) || overlaps(r_pool, r)) return KDA_ERR_ALIAS;
-    if (overlaps(r_out, r_pool)) return KDA_ERR_ALIAS;
-
-    kda::PrefillArgs a{};
-    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.scale = scale;
-    a.cu_seqlens = cu_seqlens; a.out = out;
-    a.state_pool = state_pool; a.state_idx = state_idx; a.num_slots = num_slots;
-    a.total_tokens = total_tokens; a.num_seqs = num_seqs;
-    a.num_heads = num_heads; a.head_dim_k = head_dim_k; a.head_dim_v = head_dim_v;
-    a.dtype = dtype; a.out_dtype = out_dtype;
+    kda::PrefillArgs a;
+    Range ranges[9];
+    const int st = check_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens,
+                                       out, total_tokens, num_seqs, num_slots, num_heads,
+                                       head_dim_k, head_dim_v, dtype, out_dtype, a, ranges);
+    if (st != KDA_OK || num_seqs == 0) return st;
     return launch_prefill(a, stream);
+}
+
+int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void *v,
+                               const float *g, const float *beta, float scale,
+                               float *state_pool, const int32_t *state_idx,
+                               const int32_t *cu_seqlens, void *out,
+                               int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
+                               int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
+                               int32_t dtype, int32_t out_dtype, void *workspace,
+                               size_t workspace_bytes, void *stream)
+{
+    kda::PrefillArgs a;
+    Range ranges[9];
+    const int st = check_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens,
+                                       out, total_tokens, num_seqs, num_slots, num_heads,
+                                       head_dim_k, head_dim_v, dtype, out_dtype, a, ranges);
+    if (st != KDA_OK || num_seqs == 0) return st;
+    const size_t need = kda::prefill_rr_workspace_bytes(a);
+    if (need == 0) return launch_prefill(a, stream);   // shapes without the shared-operand kernel
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
+    const Range r_ws{workspace, (uint64_t)need};
+    for (const Range &r : ranges)
+        if (overlaps(r_ws, r)) return KDA_ERR_ALIAS;
+    return finish(kda::launch_prefill_rr(a, workspace, static_cast<cudaStream_t>(stream)));
 }
 
 int kda_recurrent_decode(const void *q, const void *k, const void *v,

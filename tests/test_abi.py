@@ -235,3 +235,28 @@ def test_prefill_noalloc_validation(native):
     assert call(V=96) == native.KDA_ERR_UNSUPPORTED
     assert call(final=BASE + (1 << 24)) == native.KDA_ERR_ALIAS
     assert call(N=0) == native.KDA_OK
+
+
+def test_paged_prefill_ws_validation_and_alias(native):
+    vp = ctypes.c_void_p
+    need = native.lib.kda_chunk_prefill_workspace_bytes(2, 2, 128, 128, 1)
+
+    def call(ws, ws_bytes, **kw):
+        a = dict(q=BASE, k=BASE + (1 << 24), v=BASE + (2 << 24), g=BASE + (3 << 24),
+                 beta=BASE + (4 << 24), scale=0.125, pool=BASE + (1 << 32), idx=BASE + (5 << 24),
+                 cu=BASE + (6 << 24), out=BASE + (7 << 24), T=100, N=2, S=8, H=2, K=128, V=128,
+                 dtype=1, out_dtype=0)
+        a.update(kw)
+        return native.lib.kda_chunk_prefill_paged_ws(
+            vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
+            vp(a["pool"]), vp(a["idx"]), vp(a["cu"]), vp(a["out"]), a["T"], a["N"], a["S"],
+            a["H"], a["K"], a["V"], a["dtype"], a["out_dtype"], vp(ws), ws_bytes, None)
+
+    ws = BASE + (1 << 36)
+    assert call(ws, need, idx=None) == native.KDA_ERR_INVALID_ARG
+    assert call(ws, need, out=BASE + (1 << 32)) == native.KDA_ERR_ALIAS      # out over the pool
+    assert call(None, 0) == native.KDA_ERR_INVALID_ARG                       # workspace needed
+    assert call(ws, need - 16) == native.KDA_ERR_INVALID_ARG
+    assert call(BASE + (1 << 32) + 64, need) == native.KDA_ERR_ALIAS         # workspace over the pool
+    assert call(BASE + (5 << 24), need) == native.KDA_ERR_ALIAS              # ... over state_idx
+    assert call(None, 0, N=0) == native.KDA_OK

@@ -191,3 +191,86 @@ def test_varlen_packed_workload_sampled():
 
 def test_long_prefill_workload_sampled():
     check_case(inputs.long_prefill(), heads=[5, 27])
+
+
+# ------------------------------------------------------------ paged (slot-indexed) prefill
+
+def _run_paged_ws(case, pool_cpu, slots, out_dtype=torch.float32):
+    from kimi_delta_attention_09_gb300 import _native
+    q, k, v, g, beta = (cuda(x) for x in (case.q, case.k, case.v, case.g, case.beta))
+    pool = cuda(pool_cpu)
+    idx = torch.tensor(slots, dtype=torch.int32, device="cuda")
+    out = torch.full(v.shape, float("nan"), dtype=out_dtype, device="cuda")
+    _native.kda_chunk_prefill_paged_ws(q, k, v, g, beta, case.scale, pool, idx,
+                                       cuda(case.cu_seqlens), out, workspace_for(case))
+    torch.cuda.synchronize()
+    return out.cpu(), pool.cpu()
+
+
+def test_paged_ws_reads_and_writes_its_slots():
+    """Sequence n starts from slot state_idx[n] and its final state lands there (not in
+    slot 0, not in slot n); every other slot is bit-identical."""
+    case = inputs.prefill_case([70, 1, 130], H=2, K=128, V=128, dtype="bf16", seed=170)
+    gen = torch.Generator().manual_seed(171)
+    pool0 = (torch.randn(6, 2, 128, 128, generator=gen) * 0.05).float()
+    slots = [4, 0, 2]
+    out, pool = _run_paged_ws(case, pool0, slots)
+    case.init_state = pool0[slots].clone()
+    ref_out, ref_fin = oracle_prefill(case)
+    assert rel_err(out, ref_out) <= TOL["bf16"]
+    for n, s in enumerate(slots):
+        assert rel_err(pool[s], ref_fin[n]) <= TOL["bf16"]
+        assert not torch.equal(pool[s], pool0[s])
+    for s in (1, 3, 5):
+        assert torch.equal(pool[s].view(torch.int32), pool0[s].view(torch.int32))
+
+
+def test_paged_ws_out_of_range_slot_and_many_items():
+    """An index outside [0, S) reads and writes no slot (zero start, final state dropped);
+    40 sequences x 3 heads are more work items than clusters."""
+    lens = [(37 * i) % 150 for i in range(40)]
+    case = inputs.prefill_case(lens, H=3, K=128, V=128, dtype="bf16", seed=172)
+    gen = torch.Generator().manual_seed(173)
+    S = 48
+    pool0 = (torch.randn(S, 3, 128, 128, generator=gen) * 0.05).float()
+    slots = [(5 * i + 1) % S for i in range(40)]
+    slots[7] = S + 3       # out of range
+    slots[11] = -1         # out of range
+    out, pool = _run_paged_ws(case, pool0, slots)
+    used = [s for s in slots if 0 <= s < S]
+    case.init_state = torch.stack([pool0[s] if 0 <= s < S else torch.zeros(3, 128, 128)
+                                   for s in slots])
+    ref_out, ref_fin = oracle_prefill(case)
+    assert rel_err(out, ref_out) <= TOL["bf16"]
+    for n, s in enumerate(slots):
+        if 0 <= s < S:
+            assert rel_err(pool[s], ref_fin[n]) <= TOL["bf16"]
+    for s in range(S):
+        if s not in used:
+            assert torch.equal(pool[s].view(torch.int32), pool0[s].view(torch.int32))
+
+
+def test_paged_ws_then_paged_decode():
+    """The runner's path: a prompt through the paged cluster prefill, then token-by-token
+    decode on the same slot = the oracle over the whole sequence."""
+    from kimi_delta_attention_09_gb300 import _native
+    T0, steps, H = 150, 5, 2
+    full = inputs.prefill_case([T0 + steps], H=H, K=128, V=128, dtype="bf16", seed=174)
+    pre = inputs.PrefillCase(name="p", seed=0, q=full.q[:T0], k=full.k[:T0], v=full.v[:T0],
+                             g=full.g[:T0], beta=full.beta[:T0],
+                             cu_seqlens=torch.tensor([0, T0], dtype=torch.int32),
+                             init_state=None, scale=full.scale)
+    out_p, pool = _run_paged_ws(pre, torch.zeros(4, H, 128, 128), [3])
+    pool = pool.cuda()
+    idx = torch.tensor([3], dtype=torch.int32, device="cuda")
+    outs = [out_p]
+    for t in range(T0, T0 + steps):
+        o = torch.empty(1, H, 128, dtype=torch.float32, device="cuda")
+        sl = slice(t, t + 1)
+        _native.kda_recurrent_decode(cuda(full.q[sl]), cuda(full.k[sl]), cuda(full.v[sl]),
+                                     cuda(full.g[sl]), cuda(full.beta[sl]), full.scale, pool,
+                                     idx, o)
+        outs.append(o.cpu())
+    ref_out, ref_fin = oracle_prefill(full)
+    assert rel_err(torch.cat(outs), ref_out) <= TOL["bf16"]
+    assert rel_err(pool[3].cpu(), ref_fin[0]) <= TOL["bf16"]
