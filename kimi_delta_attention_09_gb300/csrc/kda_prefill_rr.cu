@@ -14,8 +14,10 @@
 //     gate cumsum, reference, fp16 factors [a_k; a_q] and K^^T, the A matrices
 //     (tcgen05) and the whole triangular inverse T -- and writes it to a ring of 8
 //     records per cluster in global memory (it stays in L2);
-//   * every CTA bulk-loads each record into one of two shared-memory slots and runs
-//     the serial state step of its value tile on it (S1, X, S2 = T X, S3, output).
+//   * every CTA receives each record in one of two shared-memory slots (one multicast
+//     bulk copy from the builder to all four) and runs the serial state step of its
+//     value tile on it (S1, X, S2 = T X, S3; a chunk's output rows are stored during the
+//     next chunk's S1 / X phase, by warps that are otherwise idle then).
 //
 // Hand-offs (all waits bounded; a timeout marks the state NaN):
 //   slot_free[n % 8] (builder's CTA, count 4): each CTA arms its slot n % 2 for chunk n
@@ -496,8 +498,8 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
     } else {
         // =====================================================================
         // State-step group (warps 0..7): the chunks of every work item of this cluster
-        // in order, on the records loaded into slot n % 2.  Thread 0 also issues the
-        // loads, two chunks ahead.  Warp w reaches TMEM lanes 32 (w % 4) ..; state roles:
+        // in order, on the records received in slot n % 2.  Thread 64 also arms the
+        // slots, two chunks ahead.  Warp w reaches TMEM lanes 32 (w % 4) ..; state roles:
         // key channel sc = 32 (w % 4) + lane, value columns [16 hc, +16).
         // =====================================================================
         const int sc = 32 * (warp & 3) + lane;
