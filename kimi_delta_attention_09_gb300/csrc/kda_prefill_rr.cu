@@ -78,6 +78,10 @@ struct Smem {
     static constexpr int st_tw = st_bk + C * KD * 2;         // builder: SW128 T 64 x 64 (record ta rows 0..63)
     static constexpr int st_akk = st_tw + C * C * 2;         // builder: SW128 A_kk 64 x 64
     static constexpr int st_vec = st_akk + C * C * 2;        // builder: beta, dec, pm (record layout)
+    static constexpr int st_kht = st_tw;                     // builder: SW128 K^^T 128 x 64 over T and
+                                                             // A_kk, from P2 until its bulk store read it
+    static constexpr int st_aqk = st_tw;                     // builder: SW128 A_qk 64 x 64 from the A
+                                                             // epilogue until its bulk store read it
     static constexpr int bars = st_vec + (Rec::bytes - Rec::beta);
     static constexpr int consumed = bars + Bar::count * 8;   // i64: chunks whose record this CTA has
     static constexpr int tmem = consumed + 8;                // u32
@@ -166,6 +170,8 @@ __device__ __forceinline__ void bulk_s2g(void *dst, uint32_t src, uint32_t bytes
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+// the sources of every committed bulk store have been read (shared memory is reusable)
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory"); }
 
 // ------------------------------------------------------------------ work walk
 // The chunks of a cluster: work items w = c, c + G, ... (item w = sequence w / H, head
@@ -392,8 +398,9 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                     khy[u] = b1 * fy;
                 }
                 // K^^T: these eight rows are one 16-byte chunk of key-channel rows pc0, pc0 + 1
+                // (staged in shared memory; one bulk store moves the tile to the record)
                 const int r0 = 16 * pE + 8 * hb;
-                __half *kh = reinterpret_cast<__half *>(rec + Rec::kht);
+                __half *kh = reinterpret_cast<__half *>(sm + Smem::st_kht);
                 *reinterpret_cast<uint4 *>(kh + sw128(pc0, r0, KD)) =
                     make_uint4(pack_h2(khx[0], khx[1]), pack_h2(khx[2], khx[3]),
                                pack_h2(khx[4], khx[5]), pack_h2(khx[6], khx[7]));
@@ -411,17 +418,21 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
             if (!exact_path) {
                 // ---------------- MMA A: [A_kk'; A_qk'] = [a_k; a_q] b^T
                 if (gtid == 0) {
+                    bulk_s2g(rec + Rec::kht, smem_u32(sm + Smem::st_kht), KD * C * 2);   // K^^T
+                    bulk_commit();
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < KD / 16; ++ks)
                         umma_f16(tDA, sw128_kdesc(smem_u32(aop), ks, 2 * C), sw128_kdesc(smem_u32(bop), ks, C),
                                  kIdescM128N64, ks > 0);
                     umma_commit(bar(Bar::a));
+                    bulk_wait_read_all();   // the K^^T staging is read: A_kk and A_qk may go there
                 }
-                // ---------------- A epilogue: masked, beta-scaled A_kk (shared) and A_qk (record)
+                // ---------------- A epilogue: masked, beta-scaled A_kk and A_qk (both staged)
                 //   lanes 0..63 A_kk, 64..127 A_qk; warp w: lane quadrant w % 4, columns [32 ((w / 4) % 2), +32)
                 if (!mbar_wait(bar(Bar::a), a_parity)) failed = true;
                 a_parity ^= 1u;
+                named_bar_sync(kBarBuild, kGroup);
                 tc_fence_after();
                 const int c0 = 32 * ((warp >> 2) & 1), rg = 32 * (warp & 3) + lane;
                 float av[2][16];
@@ -431,7 +442,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                 const int r = kk ? rg : rg - C;
                 const float sb = kk ? bs[r] : 1.f;
                 const int lim = kk ? r : r + 1;   // columns i < lim are kept
-                __half *dst = kk ? akk : reinterpret_cast<__half *>(aqk_g);
+                __half *dst = kk ? akk : reinterpret_cast<__half *>(sm + Smem::st_aqk);
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     uint32_t w[4];
@@ -456,10 +467,12 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                 named_bar_sync(kBarBuild, kGroup);
                 exact_pairs(a, t0, len, h, Gs, bs, akk, aqk_g, rec + Rec::kht, gtid);
             }
+            if (!exact_path) fence_proxy_async_smem();   // A_qk is read by the bulk copy
             named_bar_sync(kBarBuild, kGroup);   // A_kk complete; the G scratch is no longer read
-            if (gtid == 0) {   // [a_k; a_q] to the record
+            if (gtid == 0) {   // [a_k; a_q] (and on the fast path A_qk) to the record
                 fence_proxy_async_global();
                 bulk_s2g(rec + Rec::aop, smem_u32(aop), 2 * C * KD * 2);
+                if (!exact_path) bulk_s2g(aqk_g, smem_u32(sm + Smem::st_aqk), C * C * 2);
                 bulk_commit();
             }
 
@@ -469,6 +482,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
             if (warp == 10) solve_column_block(akk, tmh, 0, lane);
             else if (warp == 11) solve_column_block(akk, tmh, 1, lane);
             else if (warp == 12) solve_column_block(akk, tmh, 2, lane);
+            if (gtid == 0) bulk_wait_read_all();   // the A_qk staging is read: T may go there
             named_bar_sync(kBarBuild, kGroup);
             // T (zeros above its diagonal blocks) -> SW128 rows 0..63 of [T; A_qk]
             for (int e = gtid; e < C * C / 8; e += kGroup) {
