@@ -75,6 +75,19 @@ def test_more_work_items_than_clusters():
         assert torch.equal(fin[n], case.init_state[n])
 
 
+def test_many_short_ragged_sequences():
+    """40 and 70 sequences of ragged lengths (ties and empty ones included): each
+    persistent cluster walks several items of different lengths."""
+    rng = np.random.default_rng(165)
+    for n_seqs in (40, 70):
+        lens = [int(x) for x in rng.integers(0, 160, size=n_seqs)]
+        lens[3] = lens[5] = 0
+        lens[7] = lens[9] = 130
+        case = inputs.prefill_case(lens, H=2, K=128, V=128, dtype="bf16", seed=165 + n_seqs,
+                                   init_std=0.02)
+        check_case(case)
+
+
 def test_final_state_in_place_and_empty_sequences():
     case = inputs.prefill_case([0, 130, 0, 5], H=2, K=128, V=128, dtype="bf16", seed=162,
                                init_std=0.05)
