@@ -54,9 +54,9 @@ def prefill_flops_per_token_head(K=K_DIM, V=V_DIM, C=CHUNK):
     return 6 * K * V + C * (3 * K + 2 * V)
 
 
-def decode_bytes_per_seq_head(K=K_DIM, V=V_DIM, es=2):
-    """State read + write (fp32) + q, k, v, o (bf16) + g (fp32) + beta."""
-    return 2 * 4 * K * V + (2 * K + V) * es + 4 * K + 4 + V * es
+def decode_bytes_per_seq_head(K=K_DIM, V=V_DIM, es=2, state_es=4):
+    """State read + write (fp32, or bf16 with state_es = 2) + q, k, v, o (bf16) + g (fp32) + beta."""
+    return 2 * state_es * K * V + (2 * K + V) * es + 4 * K + 4 + V * es
 
 
 # ------------------------------------------------------------------ helpers
@@ -265,14 +265,18 @@ def measure_e2e(args, case, bufs, stream, flush, world):
     return times, h2d, d2h, n * segments   # one prefill kernel per piece
 
 
-def measure_decode(args, dev, stream, flush, world):
+def measure_decode(args, dev, stream, flush, world, bf16_state=False):
     """Device time per step of kda_recurrent_decode on the paged-decode workload
-    (64 steps carrying the state in place through a 1024-slot fp32 pool)."""
+    (64 steps carrying the state in place through a 1024-slot fp32 pool); with
+    bf16_state, of kda_recurrent_decode_bf16_state on the same pool stored in bf16."""
     import torch
     from kimi_delta_attention_09_gb300 import _native, inputs
     dcase = inputs.paged_decode(steps=DECODE_STEPS)
     N = min(args.decode_seqs, dcase.N)
     pool = dcase.pool.to(dev)
+    if bf16_state:
+        pool = pool.to(torch.bfloat16)
+    fn = _native.kda_recurrent_decode_bf16_state if bf16_state else _native.kda_recurrent_decode
     idx = dcase.state_idx[:N].contiguous().to(dev)
     steps = [tuple(x[:N].contiguous().to(dev) for x in (s.q, s.k, s.v, s.g, s.beta))
              for s in dcase.steps]
@@ -283,14 +287,16 @@ def measure_decode(args, dev, stream, flush, world):
     def step():
         sq, sk, sv, sg, sb = steps[counter[0] % DECODE_STEPS]
         counter[0] += 1
-        _native.kda_recurrent_decode(sq, sk, sv, sg, sb, dcase.scale, pool, idx, dout, stream)
+        fn(sq, sk, sv, sg, sb, dcase.scale, pool, idx, dout, stream)
 
     barrier(world)
     times = time_steps(step, DECODE_STEPS if args.only != "decode" else max(args.steps, 1),
                        args.warmup, stream, flush)
     barrier(world)
-    d_bytes = N * H * decode_bytes_per_seq_head()
+    d_bytes = N * H * decode_bytes_per_seq_head(state_es=2 if bf16_state else 4)
     name = dcase.name if N == dcase.N else dcase.name.replace("N256", f"N{N}")
+    if bf16_state:
+        name += "_bf16_state"
     return name, N, times, d_bytes
 
 
@@ -362,6 +368,19 @@ def run_ours(args, rank, world, local):
             "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": round(d_gbs, 1),
                          "peak": peak_hbm, "unit": "GB/s", "frac": round(d_gbs / peak_hbm, 4),
                          "traffic": traffic.get("decode_paged")}}
+        name, N, dtimes, d_bytes = measure_decode(args, dev, stream, flush, world, bf16_state=True)
+        d_ms = statistics.mean(dtimes)
+        d_ms_max = max_over_ranks(d_ms, world)
+        d_gbs = d_bytes / (d_ms * 1e-3) / 1e9
+        launches += len(dtimes)
+        line["decode_bf16_state"] = {
+            "workload": name, "metric": "state GB/s",
+            "value": round(world * d_bytes / (d_ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(d_ms_max, 5), "steps": len(dtimes),
+            "algorithmic_bytes_per_step": d_bytes,
+            "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel (bf16 state)",
+                         "achieved": round(d_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                         "frac": round(d_gbs / peak_hbm, 4), "traffic": None}}
     line["gpu_launches"] = launches
     if rank == 0:
         print(json.dumps(line), flush=True)

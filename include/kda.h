@@ -26,7 +26,8 @@
  *                            form runs on the shared-operand kernel.
  *   kda_recurrent_decode  -- one token per sequence against the state held in a
  *                            paged pool slot, updated in place (state slots keyed
- *                            by per-sequence indices, PR #122 block B2).
+ *                            by per-sequence indices, PR #122 block B2); its
+ *                            _bf16_state form keeps the pool in bf16.
  *
  * Conventions for every call
  * --------------------------
@@ -62,7 +63,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 2
+#define KDA_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define KDA_API __attribute__((visibility("default")))
@@ -268,6 +269,29 @@ KDA_API int kda_recurrent_decode(const void *q, const void *k, const void *v,
                                  int32_t num_seqs, int32_t num_slots, int32_t num_heads,
                                  int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
                                  int32_t out_dtype, void *stream);
+
+/*
+ * kda_recurrent_decode over a pool stored in bf16: the same step, the same
+ * arguments, with state_pool [num_slots, H, K, V] of bf16 elements.
+ *
+ * The state's element type is a configuration of the model runner (vllm.cpp PR #122,
+ * block B3: the conv cache dtype mirrors kda_state_dtype); the pages give no rule for
+ * how a narrower state is used, and the one taken here is storage only: the selected
+ * state is read into fp32, the step runs in fp32 exactly as with an fp32 pool, the
+ * output is read from the fp32 updated state, and only the stored state is rounded
+ * (to nearest, ties to even).  Each step thus reads and writes half the bytes and
+ * rounds the carried state once (relative error <= 2^-9 per element and step; the
+ * same pages warn that bf16 rounding inside the recurrence can destabilise it, so
+ * this form is opt-in).  Slots outside state_idx are left bit-identical; the errors,
+ * alignment and aliasing rules are those of kda_recurrent_decode (the pool's byte
+ * range is num_slots * H * K * V * 2).
+ */
+KDA_API int kda_recurrent_decode_bf16_state(const void *q, const void *k, const void *v,
+                                            const float *g, const float *beta, float scale,
+                                            void *state_pool, const int32_t *state_idx, void *out,
+                                            int32_t num_seqs, int32_t num_slots, int32_t num_heads,
+                                            int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                                            int32_t out_dtype, void *stream);
 
 #ifdef __cplusplus
 }

@@ -12,13 +12,14 @@ from __future__ import annotations
 __all__ = ["chunk_prefill", "chunk_prefill_paged", "chunk_prefill_from_host", "recurrent_decode",
            "prefill_workspace", "kda_chunk_prefill", "kda_chunk_prefill_ws",
            "kda_chunk_prefill_paged_ws", "kda_chunk_prefill_noalloc",
-           "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_paged", "kda_recurrent_decode"]
+           "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_paged", "kda_recurrent_decode",
+           "kda_recurrent_decode_bf16_state"]
 
 
 def __getattr__(name):
     if name in ("kda_chunk_prefill", "kda_chunk_prefill_ws", "kda_chunk_prefill_workspace_bytes",
                 "kda_chunk_prefill_paged", "kda_chunk_prefill_paged_ws", "kda_chunk_prefill_noalloc",
-                "kda_recurrent_decode", "KdaError"):
+                "kda_recurrent_decode", "kda_recurrent_decode_bf16_state", "KdaError"):
         from . import _native
         return getattr(_native, name)
     raise AttributeError(name)
@@ -101,13 +102,19 @@ def chunk_prefill_paged(q, k, v, g, beta, state_pool, state_idx, scale=None, cu_
 
 def recurrent_decode(q, k, v, g, beta, state_pool, state_idx, scale=None, out_dtype=None,
                      stream=None):
-    """One KDA decode step; ``state_pool`` is updated in place at ``state_idx``."""
+    """One KDA decode step; ``state_pool`` is updated in place at ``state_idx``.
+
+    An fp32 pool runs ``kda_recurrent_decode``; a bf16 pool runs
+    ``kda_recurrent_decode_bf16_state`` (fp32 step, the stored state rounded to bf16)."""
     import torch
     from . import _native
     if scale is None:
         scale = q.shape[-1] ** -0.5
     out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
-    _native.kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out, stream)
+    if state_pool.dtype == torch.bfloat16:
+        _native.kda_recurrent_decode_bf16_state(q, k, v, g, beta, scale, state_pool, state_idx, out, stream)
+    else:
+        _native.kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out, stream)
     return out
 
 

@@ -19,12 +19,12 @@ KDA_ERR_ALIAS = -3
 KDA_ERR_CUDA = -4
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
             "kda_chunk_prefill", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_ws",
             "kda_chunk_prefill_noalloc", "kda_chunk_prefill_paged_ws",
-            "kda_chunk_prefill_paged", "kda_recurrent_decode")
+            "kda_chunk_prefill_paged", "kda_recurrent_decode", "kda_recurrent_decode_bf16_state")
 
 
 class KdaError(RuntimeError):
@@ -67,6 +67,9 @@ def _load() -> ctypes.CDLL:
     lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp,
                                          i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_recurrent_decode.restype = ctypes.c_int
+    lib.kda_recurrent_decode_bf16_state.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp,
+                                                    i32, i32, i32, i32, i32, i32, i32, vp]
+    lib.kda_recurrent_decode_bf16_state.restype = ctypes.c_int
     if lib.kda_abi_version() != ABI_VERSION:
         raise RuntimeError(f"libkda.so ABI {lib.kda_abi_version()} != expected {ABI_VERSION}")
     return lib
@@ -276,9 +279,7 @@ def kda_chunk_prefill_paged_ws(q, k, v, g, beta, scale, state_pool, state_idx, c
     _check("kda_chunk_prefill_paged_ws", rc)
 
 
-def kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out,
-                         stream=None) -> None:
-    """Enqueue ``kda_recurrent_decode``: q [N, H, K], v [N, H, V], pool [S, H, K, V]."""
+def _decode(fn, q, k, v, g, beta, scale, state_pool, state_idx, out, pool_dtype, stream):
     N, H, K = q.shape
     V = v.shape[-1]
     S = state_pool.shape[0]
@@ -289,13 +290,29 @@ def kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out,
     _need(k.shape == q.shape and g.shape == q.shape, "q, k, g must be [N, H, K]")
     _need(v.shape[:2] == (N, H) and out.shape == v.shape, "v, out must be [N, H, V]")
     _need(beta.shape == (N, H), "beta must be [N, H]")
-    _need(tuple(state_pool.shape[1:]) == (H, K, V) and state_pool.dtype == torch.float32,
-          "state_pool must be fp32 [S, H, K, V]")
+    _need(tuple(state_pool.shape[1:]) == (H, K, V) and state_pool.dtype == pool_dtype,
+          f"state_pool must be {pool_dtype} [S, H, K, V]")
     _need(state_idx.dtype == torch.int32 and state_idx.numel() == N, "state_idx must be int32 [N]")
     _need(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v must share one dtype")
     _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g, beta must be fp32")
-    rc = lib.kda_recurrent_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
-                                  _ptr(state_pool), _ptr(state_idx), _ptr(out),
-                                  N, S, H, K, V, _dtype_code(q), _dtype_code(out),
-                                  _stream_handle(stream))
-    _check("kda_recurrent_decode", rc)
+    rc = getattr(lib, fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                          _ptr(state_pool), _ptr(state_idx), _ptr(out),
+                          N, S, H, K, V, _dtype_code(q), _dtype_code(out),
+                          _stream_handle(stream))
+    _check(fn, rc)
+
+
+def kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out,
+                         stream=None) -> None:
+    """Enqueue ``kda_recurrent_decode``: q [N, H, K], v [N, H, V], fp32 pool [S, H, K, V]."""
+    import torch
+    _decode("kda_recurrent_decode", q, k, v, g, beta, scale, state_pool, state_idx, out,
+            torch.float32, stream)
+
+
+def kda_recurrent_decode_bf16_state(q, k, v, g, beta, scale, state_pool, state_idx, out,
+                                    stream=None) -> None:
+    """Enqueue ``kda_recurrent_decode_bf16_state``: the same step on a bf16 pool [S, H, K, V]."""
+    import torch
+    _decode("kda_recurrent_decode_bf16_state", q, k, v, g, beta, scale, state_pool, state_idx, out,
+            torch.bfloat16, stream)

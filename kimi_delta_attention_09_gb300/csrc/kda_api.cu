@@ -312,12 +312,12 @@ int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void *v,
     return finish(kda::launch_prefill_rr(a, workspace, static_cast<cudaStream_t>(stream)));
 }
 
-int kda_recurrent_decode(const void *q, const void *k, const void *v,
-                         const float *g, const float *beta, float scale,
-                         float *state_pool, const int32_t *state_idx, void *out,
-                         int32_t num_seqs, int32_t num_slots, int32_t num_heads,
-                         int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                         int32_t out_dtype, void *stream)
+static int recurrent_decode(const void *q, const void *k, const void *v,
+                            const float *g, const float *beta, float scale,
+                            void *state_pool, int32_t state_dtype, const int32_t *state_idx, void *out,
+                            int32_t num_seqs, int32_t num_slots, int32_t num_heads,
+                            int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                            int32_t out_dtype, void *stream)
 {
     if (num_seqs < 0 || num_slots < 0 || num_heads < 1 || !std::isfinite(scale))
         return KDA_ERR_INVALID_ARG;
@@ -333,10 +333,11 @@ int kda_recurrent_decode(const void *q, const void *k, const void *v,
     const uint64_t K = (uint64_t)head_dim_k, V = (uint64_t)head_dim_v;
     const uint64_t es = dtype == KDA_DTYPE_BF16 ? 2 : 4;
     const uint64_t eo = out_dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const uint64_t ep = state_dtype == KDA_DTYPE_BF16 ? 2 : 4;
     const Range in[] = {{q, N * H * K * es}, {k, N * H * K * es}, {v, N * H * V * es},
                         {g, N * H * K * 4}, {beta, N * H * 4}, {state_idx, N * 4}};
     const Range r_out{out, N * H * V * eo};
-    const Range r_pool{state_pool, (uint64_t)num_slots * H * K * V * 4};
+    const Range r_pool{state_pool, (uint64_t)num_slots * H * K * V * ep};
     for (const Range &r : in)
         if (overlaps(r_out, r) || overlaps(r_pool, r)) return KDA_ERR_ALIAS;
     if (overlaps(r_out, r_pool)) return KDA_ERR_ALIAS;
@@ -346,8 +347,32 @@ int kda_recurrent_decode(const void *q, const void *k, const void *v,
     a.pool = state_pool; a.state_idx = state_idx; a.out = out;
     a.num_seqs = num_seqs; a.num_slots = num_slots; a.num_heads = num_heads;
     a.head_dim_k = head_dim_k; a.head_dim_v = head_dim_v; a.dtype = dtype;
-    a.out_dtype = out_dtype;
+    a.out_dtype = out_dtype; a.state_dtype = state_dtype;
     return finish(kda::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+int kda_recurrent_decode(const void *q, const void *k, const void *v,
+                         const float *g, const float *beta, float scale,
+                         float *state_pool, const int32_t *state_idx, void *out,
+                         int32_t num_seqs, int32_t num_slots, int32_t num_heads,
+                         int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                         int32_t out_dtype, void *stream)
+{
+    return recurrent_decode(q, k, v, g, beta, scale, state_pool, KDA_DTYPE_F32, state_idx, out,
+                            num_seqs, num_slots, num_heads, head_dim_k, head_dim_v, dtype,
+                            out_dtype, stream);
+}
+
+int kda_recurrent_decode_bf16_state(const void *q, const void *k, const void *v,
+                                    const float *g, const float *beta, float scale,
+                                    void *state_pool, const int32_t *state_idx, void *out,
+                                    int32_t num_seqs, int32_t num_slots, int32_t num_heads,
+                                    int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                                    int32_t out_dtype, void *stream)
+{
+    return recurrent_decode(q, k, v, g, beta, scale, state_pool, KDA_DTYPE_BF16, state_idx, out,
+                            num_seqs, num_slots, num_heads, head_dim_k, head_dim_v, dtype,
+                            out_dtype, stream);
 }
 
 }  // extern "C"

@@ -18,6 +18,15 @@
 // a warp reads four 128-byte row segments per instruction (fully coalesced) and
 // every thread has K/16 independent 16-byte loads in flight before it computes.
 // The work is HBM-bound (K*V*8 bytes of state per (n, h) against ~7 K*V flops).
+//
+// State storage: fp32, or bf16 (the pool's element type as a configuration of the
+// state dtype, vllm.cpp PR #122 "fold Kimi-Linear onto the shared paged runner",
+// block B3, kda_state_dtype).  A bf16 pool is read into fp32, the step runs in fp32
+// exactly as for an fp32 pool, the output is read from the fp32 updated state, and
+// the state is rounded to nearest-even bf16 only where it is stored: half the bytes
+// per step, one rounding of the carried state per step.  Its kernel takes 64 columns
+// per CTA (8 per thread, one 16-byte load and store per row), so that a CTA moves as
+// many bytes as on an fp32 pool.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -52,7 +61,7 @@ kda_decode_kernel(DecodeArgs a)
     }
 
     float4 *S = reinterpret_cast<float4 *>(
-        a.pool + ((int64_t)slot * H + h) * (int64_t)(K * V) + col0);
+        static_cast<float *>(a.pool) + ((int64_t)slot * H + h) * (int64_t)(K * V) + col0);
     const Tin *kp = static_cast<const Tin *>(a.k) + (n * H + h) * K;
     const Tin *qp = static_cast<const Tin *>(a.q) + (n * H + h) * K;
     const float *gp = a.g + (n * H + h) * K;
@@ -130,11 +139,140 @@ kda_decode_kernel(DecodeArgs a)
     }
 }
 
+constexpr int kDecCols16 = 64;   // V columns per CTA on a bf16 pool
+
+// The same step on a bf16 pool: thread t owns columns [8 (t % 8), +8) of the CTA's
+// 64 on rows t / 8 + 16 j; the state is widened to fp32 on load and rounded to
+// nearest-even bf16 on store.
+template <typename Tin, typename Tout, int K, int V>
+__global__ void __launch_bounds__(kDecThreads, 5)
+kda_decode_bf16_state_kernel(DecodeArgs a)
+{
+    constexpr int kSlices = V / kDecCols16;
+    constexpr int kRowsPerThread = K / 16;
+    const int tid = threadIdx.x;
+    const int cg = tid & 7;          // column group (8 columns)
+    const int rg = tid >> 3;         // row group 0..15
+    const int64_t n = blockIdx.x / kSlices;
+    const int slice = blockIdx.x % kSlices;
+    const int h = blockIdx.y;
+    const int H = a.num_heads;
+    const int col0 = slice * kDecCols16 + cg * 8;
+
+    const int32_t slot = a.state_idx[n];
+    Tout *out = static_cast<Tout *>(a.out) + (n * H + h) * V + col0;
+    if (slot < 0 || slot >= a.num_slots) {           // bounds check: touch no slot
+        if (rg == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) out[i] = from_f32<Tout>(0.f);
+        }
+        return;
+    }
+
+    __nv_bfloat16 *S = static_cast<__nv_bfloat16 *>(a.pool) + ((int64_t)slot * H + h) * (int64_t)(K * V) + col0;
+    const Tin *kp = static_cast<const Tin *>(a.k) + (n * H + h) * K;
+    const Tin *qp = static_cast<const Tin *>(a.q) + (n * H + h) * K;
+    const float *gp = a.g + (n * H + h) * K;
+
+    uint4 raw[kRowsPerThread];
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; ++j)
+        raw[j] = __ldcs(reinterpret_cast<const uint4 *>(S + (int64_t)(rg + 16 * j) * V));
+
+    float kr[kRowsPerThread], qr[kRowsPerThread], dr[kRowsPerThread];
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; ++j) {
+        const int c = rg + 16 * j;
+        kr[j] = to_f32(kp[c]);
+        qr[j] = to_f32(qp[c]);
+        dr[j] = expf(gp[c]);
+    }
+
+    // the decayed row, widened again where it is needed (keeps 8 registers per row, not 16)
+    auto decayed = [&](int j, float (&x)[8]) {
+        const __nv_bfloat162 *w = reinterpret_cast<const __nv_bfloat162 *>(&raw[j]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 f = __bfloat1622float2(w[e]);
+            x[2 * e] = f.x * dr[j];
+            x[2 * e + 1] = f.y * dr[j];
+        }
+    };
+    float pk[8], pq[8], kq = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) pk[i] = pq[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; ++j) {
+        float x[8];
+        decayed(j, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { pk[i] += x[i] * kr[j]; pq[i] += x[i] * qr[j]; }
+        kq += kr[j] * qr[j];
+    }
+#pragma unroll
+    for (int off = 8; off <= 16; off <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            pk[i] += __shfl_xor_sync(0xffffffffu, pk[i], off);
+            pq[i] += __shfl_xor_sync(0xffffffffu, pq[i], off);
+        }
+        kq += __shfl_xor_sync(0xffffffffu, kq, off);
+    }
+    __shared__ float red[kDecThreads / 32][8][17];
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane < 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { red[warp][lane][i] = pk[i]; red[warp][lane][8 + i] = pq[i]; }
+        red[warp][lane][16] = kq;
+    }
+    __syncthreads();
+    float u[8], qs[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[i] = qs[i] = 0.f;
+    kq = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecThreads / 32; ++w) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { u[i] += red[w][cg][i]; qs[i] += red[w][cg][8 + i]; }
+        kq += red[w][cg][16];
+    }
+
+    const float beta = a.beta[n * H + h];
+    const Tin *vp = static_cast<const Tin *>(a.v) + (n * H + h) * V + col0;
+    float d[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = beta * (to_f32(vp[i]) - u[i]);
+
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; ++j) {
+        float x[8];
+        decayed(j, x);
+        uint4 w;
+        uint32_t *pw = reinterpret_cast<uint32_t *>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(x[2 * e] + kr[j] * d[2 * e],
+                                                      x[2 * e + 1] + kr[j] * d[2 * e + 1]);
+            pw[e] = *reinterpret_cast<uint32_t *>(&b2);
+        }
+        __stcs(reinterpret_cast<uint4 *>(S + (int64_t)(rg + 16 * j) * V), w);
+    }
+    if (rg == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) out[i] = from_f32<Tout>(a.scale * (qs[i] + kq * d[i]));
+    }
+}
+
 template <typename Tin, typename Tout, int K, int V>
 cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream)
 {
-    dim3 grid((unsigned)((int64_t)a.num_seqs * (V / kDecCols)), (unsigned)a.num_heads);
-    kda_decode_kernel<Tin, Tout, K, V><<<grid, kDecThreads, 0, stream>>>(a);
+    if (a.state_dtype == kDtypeBF16) {
+        dim3 grid((unsigned)((int64_t)a.num_seqs * (V / kDecCols16)), (unsigned)a.num_heads);
+        kda_decode_bf16_state_kernel<Tin, Tout, K, V><<<grid, kDecThreads, 0, stream>>>(a);
+    } else {
+        dim3 grid((unsigned)((int64_t)a.num_seqs * (V / kDecCols)), (unsigned)a.num_heads);
+        kda_decode_kernel<Tin, Tout, K, V><<<grid, kDecThreads, 0, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 

@@ -49,10 +49,10 @@ struct DecodeArgs {
     const void *q, *k, *v;        // [N, H, K] / [N, H, V], dtype
     const float *g, *beta;        // [N, H, K], [N, H]
     float scale;
-    float *pool;                  // [S, H, K, V]
+    void *pool;                   // [S, H, K, V], state_dtype (fp32 or bf16 storage)
     const int32_t *state_idx;     // [N]
     void *out;                    // [N, H, V], out_dtype
-    int32_t num_seqs, num_slots, num_heads, head_dim_k, head_dim_v, dtype, out_dtype;
+    int32_t num_seqs, num_slots, num_heads, head_dim_k, head_dim_v, dtype, out_dtype, state_dtype;
 };
 
 constexpr int kDtypeF32 = 0;

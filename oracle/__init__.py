@@ -11,6 +11,10 @@ Contents
 * ``prefill`` / ``decode``: ctypes front-end for ``kda_oracle.c``, the token-by-token
   fp64 recurrence (the plain definition of the gated delta rule with a per-key-channel
   decay; see the header of ``kda_oracle.c`` for the citations and the step order).
+* ``decode_bf16_state``: the decode step on a pool stored in bf16 (the state's element
+  type as a runner configuration, vllm.cpp PR #122, block B3, kda_state_dtype): the
+  fp64 step of ``decode`` on the stored values, the output from the unrounded updated
+  state, each updated slot then rounded to the nearest bf16 (``round_to_bf16``).
 * ``chunked.prefill_chunked``: a second statement of the same definition, evaluated
   chunk by chunk (numpy, fp64), used to pin the chunk algebra that a chunked
   implementation relies on.
@@ -144,4 +148,30 @@ def decode(q, k, v, g, beta, scale: float, pool, state_idx, nthreads: int | None
         int(nthreads or default_threads()))
     if rc != 0:
         raise ValueError(f"kda_oracle_decode failed with status {rc}")
+    return out
+
+
+def round_to_bf16(x) -> np.ndarray:
+    """Nearest bfloat16 value of each element (8 significant bits, ties to even), computed
+    exactly from fp64: with |x| = m 2^e, 1/2 <= m < 1, the bf16 spacing there is 2^(e-8)
+    (2^-133 below the smallest normal 2^-126); a result of 2^128 or more (past the
+    largest bf16, 2^128 - 2^120) is infinite.  Returned as float64."""
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    e = np.maximum(e, -125)
+    y = np.ldexp(np.rint(np.ldexp(x, 8 - e)), e - 8)
+    return np.where(np.abs(y) >= 2.0 ** 128, np.copysign(np.inf, y), y)
+
+
+def decode_bf16_state(q, k, v, g, beta, scale: float, pool, state_idx, nthreads: int | None = None):
+    """One decode step on a pool stored in bf16.
+
+    pool: [S, H, K, V] float64 numpy array holding bf16 values, updated IN PLACE at the
+    slots state_idx: the step of ``decode`` in fp64, then each updated slot rounded to
+    the nearest bf16.  The output is read from the unrounded updated state.  Returns
+    out [N, H, V].
+    """
+    out = decode(q, k, v, g, beta, scale, pool, state_idx, nthreads)
+    for s in np.unique(_i64(state_idx)):
+        pool[s] = round_to_bf16(pool[s])
     return out

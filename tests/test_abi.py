@@ -52,7 +52,7 @@ def test_header_compiles_as_c(tmp_path):
 
 
 def test_status_strings(native):
-    assert native.lib.kda_abi_version() == 2
+    assert native.lib.kda_abi_version() == 3
     for code, name in [(0, "KDA_OK"), (-1, "KDA_ERR_INVALID_ARG"), (-2, "KDA_ERR_UNSUPPORTED"),
                        (-3, "KDA_ERR_ALIAS"), (-4, "KDA_ERR_CUDA")]:
         assert native.status_string(code) == name
@@ -158,6 +158,32 @@ def test_decode_argument_validation_and_alias(native):
     assert _decode(native, out=BASE + (1 << 32) + 4096) == native.KDA_ERR_ALIAS
     assert _decode(native, pool=BASE + (3 << 24)) == native.KDA_ERR_ALIAS
     assert _decode(native, idx=BASE + (1 << 32) + 64) == native.KDA_ERR_ALIAS
+
+
+def _decode_bf16_state(native, **kw):
+    a = dict(q=BASE, k=BASE + (1 << 24), v=BASE + (2 << 24), g=BASE + (3 << 24),
+             beta=BASE + (4 << 24), scale=0.125, pool=BASE + (1 << 32), idx=BASE + (6 << 24),
+             out=BASE + (7 << 24), N=4, S=8, H=2, K=128, V=128, dtype=1, out_dtype=1)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return native.lib.kda_recurrent_decode_bf16_state(
+        vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
+        vp(a["pool"]), vp(a["idx"]), vp(a["out"]), a["N"], a["S"], a["H"], a["K"], a["V"],
+        a["dtype"], a["out_dtype"], None)
+
+
+def test_decode_bf16_state_argument_validation_and_alias(native):
+    assert _decode_bf16_state(native, idx=None) == native.KDA_ERR_INVALID_ARG
+    assert _decode_bf16_state(native, pool=None) == native.KDA_ERR_INVALID_ARG
+    assert _decode_bf16_state(native, pool=BASE + (1 << 32) + 8) == native.KDA_ERR_INVALID_ARG
+    assert _decode_bf16_state(native, V=96) == native.KDA_ERR_UNSUPPORTED
+    assert _decode_bf16_state(native, dtype=7) == native.KDA_ERR_UNSUPPORTED
+    assert _decode_bf16_state(native, N=0) == native.KDA_OK
+    # the bf16 pool spans S H K V * 2 bytes: its last 16 bytes still alias the output
+    pool_bytes = 8 * 2 * 128 * 128 * 2
+    assert _decode_bf16_state(native, out=BASE + (1 << 32) + pool_bytes - 16) == native.KDA_ERR_ALIAS
+    assert _decode_bf16_state(native, pool=BASE + (3 << 24)) == native.KDA_ERR_ALIAS
+    assert _decode_bf16_state(native, idx=BASE + (1 << 32) + 64) == native.KDA_ERR_ALIAS
 
 
 def test_binding_refuses_missing_library(tmp_path, monkeypatch):

@@ -343,3 +343,71 @@ def test_pins_catch_planted_mistakes():
             assert caught, f"no pin fails for the planted mistake '{name}'"
     finally:
         shutil.rmtree(tmpdir, ignore_errors=True)
+
+
+# ------------------------------------------------------------------ bf16 state storage
+
+def test_round_to_bf16_equals_the_fp32_to_bf16_conversion():
+    """Every fp32 value (normal and subnormal, both signs, ties included) rounds to the
+    bf16 value torch's round-to-nearest-even conversion gives."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 2 ** 32, size=200_000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    ties = (np.arange(1, 5000, dtype=np.uint32) << 16 | 0x8000).view(np.float32)   # exact midpoints
+    x = np.concatenate([x, ties, -ties, np.float32([0.0, 1e-45, -1e-45, 1.1754944e-38])])
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.round_to_bf16(x.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_round_to_bf16_ties_to_even():
+    u = 2.0 ** -8   # half the bf16 step at 1
+    got = oracle.round_to_bf16(np.array([1 + u, 1 + 3 * u, 1 + 2 * u, -(1 + u), 2 - u, 3.0]))
+    assert got.tolist() == [1.0, 1 + 4 * u, 1 + 2 * u, -1.0, 2.0, 3.0]
+
+
+def _bf16_case(seed, K=8, V=6, S=5):
+    rng = np.random.default_rng(seed)
+    pool = oracle.round_to_bf16(rng.standard_normal((S, 2, K, V)) * 0.3)
+    q, k = rng.standard_normal((2, 2, 2, K))
+    v = rng.standard_normal((2, 2, V))
+    g = -0.2 * rng.random((2, 2, K))
+    beta = rng.random((2, 2))
+    return pool, q, k, v, g, beta, np.array([3, 0])
+
+
+def test_bf16_state_decode_pins():
+    # beta = 0, g = 0: the state is left as stored and the output reads it as it is
+    pool, q, k, v, g, beta, idx = _bf16_case(1)
+    start = pool.copy()
+    out = oracle.decode_bf16_state(q, k, v, 0 * g, 0 * beta, 0.5, pool, idx)
+    assert np.array_equal(pool, start)
+    for n, s in enumerate(idx):
+        assert np.allclose(out[n], 0.5 * np.einsum("hkv,hk->hv", start[s], q[n]), rtol=1e-14, atol=1e-14)
+    # a unit key with beta = 1 and no decay replaces that key row by v exactly (v on the
+    # bf16 grid), every other row and slot untouched
+    pool, q, k, v, g, beta, idx = _bf16_case(2)
+    start = pool.copy()
+    k = np.zeros_like(k)
+    k[:, :, 5] = 1.0
+    v = oracle.round_to_bf16(v)
+    oracle.decode_bf16_state(q, k, v, 0 * g, np.ones_like(beta), 0.5, pool, idx)
+    for n, s in enumerate(idx):
+        assert np.array_equal(pool[s][:, 5], v[n])
+        assert np.array_equal(np.delete(pool[s], 5, axis=1), np.delete(start[s], 5, axis=1))
+    for s in (1, 2, 4):
+        assert np.array_equal(pool[s], start[s])
+    # a general step: the stored state is on the bf16 grid, within half a bf16 step of the
+    # fp64 step, and the output is the fp64 step's
+    pool, q, k, v, g, beta, idx = _bf16_case(3)
+    exact = pool.copy()
+    out_exact = oracle.decode(q, k, v, g, beta, 0.5, exact, idx)
+    out = oracle.decode_bf16_state(q, k, v, g, beta, 0.5, pool, idx)
+    assert np.array_equal(out, out_exact)
+    assert np.array_equal(oracle.round_to_bf16(pool), pool)
+    _, e = np.frexp(exact)
+    half_step = np.ldexp(1.0, np.maximum(e, -125) - 9)
+    assert (np.abs(pool - exact) <= half_step).all()
+    assert not np.array_equal(pool[idx], exact[idx])   # the rounding did happen
