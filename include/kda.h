@@ -39,7 +39,7 @@
  *  * dtype (KDA_DTYPE_*) is the element type of q, k and v; out_dtype that of out
  *    (either may be fp32 or bf16; an fp32 out suits an fp32 residual stream, and a
  *    bf16 out holds exactly the fp32 result rounded to nearest).  g, beta and all
- *    states are fp32.  g is the NATURAL-log gate (g <= 0 for a decay); the kernels
+ *    states are fp32, except the bf16 pool of kda_recurrent_decode_bf16_state.  g is the NATURAL-log gate (g <= 0 for a decay); the kernels
  *    work in exp2 space internally.  Accumulation is fp32.
  *  * The caller owns every buffer.  The library allocates no device or host memory,
  *    keeps no per-call state, and synchronises nothing: all work is enqueued on
