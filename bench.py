@@ -380,7 +380,8 @@ def run_ours(args, rank, world, local):
             "algorithmic_bytes_per_step": d_bytes,
             "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel (bf16 state)",
                          "achieved": round(d_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
-                         "frac": round(d_gbs / peak_hbm, 4), "traffic": None}}
+                         "frac": round(d_gbs / peak_hbm, 4),
+                         "traffic": traffic.get("decode_bf16_state_paged")}}
     line["gpu_launches"] = launches
     if rank == 0:
         print(json.dumps(line), flush=True)
