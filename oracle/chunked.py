@@ -76,3 +76,49 @@ def prefill_chunked(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, c
                 out[s:e, hh] = o
             final[n, hh] = h
     return out, final
+
+
+def prefill_segmented(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, chunk=64,
+                      segments=2):
+    """Same contract as ``oracle.prefill``, evaluated with each sequence split in time.
+
+    The chunk step above is linear in (h, v).  Each sequence's chunks are split into
+    ``segments`` runs of consecutive chunks.  Every run is evaluated on its own, from a
+    zero state, carrying next to it a K x K state Phi that starts at the identity and
+    takes the same chunk step with v = 0 (the homogeneous part): after chunk n, Phi is
+    the map from the run's start state to the state there, and the output that step
+    gives for Phi (an L x K matrix Psi_n) maps the run's start state to the part of the
+    chunk's output the zero start left out.  Then, in order of the runs,
+
+        h_start(p + 1) = Phi_end(p) h_start(p) + h_end(p),    h_start(0) = init,
+
+    and every chunk's output gains Psi_n h_start(p).  The result is the recurrence's,
+    in exact arithmetic, for any split; only the order of evaluation differs.
+    """
+    q, k, v, g, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
+    T, H, K = q.shape
+    V = v.shape[-1]
+    cu = np.asarray([0, T] if cu_seqlens is None else cu_seqlens, dtype=np.int64)
+    N = cu.shape[0] - 1
+    out = np.zeros((T, H, V))
+    final = np.zeros((N, H, K, V))
+    for n in range(N):
+        bos, eos = int(cu[n]), int(cu[n + 1])
+        starts = list(range(bos, eos, chunk))
+        runs = [r for r in np.array_split(np.arange(len(starts)), max(1, segments)) if r.size]
+        for hh in range(H):
+            h_start = (np.zeros((K, V)) if init_state is None
+                       else np.array(init_state[n, hh], dtype=np.float64))
+            for run in runs:
+                h_loc, phi = np.zeros((K, V)), np.eye(K)
+                for ci in run:
+                    s = starts[ci]
+                    e = min(s + chunk, eos)
+                    args = (q[s:e, hh], k[s:e, hh])
+                    o_loc, h_loc_next = _chunk(*args, v[s:e, hh], g[s:e, hh], beta[s:e, hh], h_loc, scale)
+                    psi, phi_next = _chunk(*args, np.zeros((e - s, K)), g[s:e, hh], beta[s:e, hh], phi, scale)
+                    out[s:e, hh] = o_loc + psi @ h_start
+                    h_loc, phi = h_loc_next, phi_next
+                h_start = phi @ h_start + h_loc
+            final[n, hh] = h_start
+    return out, final

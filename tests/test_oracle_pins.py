@@ -248,6 +248,26 @@ def test_chunked_restatement_equals_recurrence(chunk):
     np.testing.assert_allclose(final_c, final, rtol=0, atol=1e-11 * np.abs(final).max())
 
 
+@pytest.mark.parametrize("segments", [1, 2, 3, 5])
+def test_segmented_restatement_equals_recurrence(segments):
+    """Each sequence split in time into runs evaluated from a zero state, joined by the
+    affine combine of their end maps: the recurrence's result for any split."""
+    rng = np.random.default_rng(30 + segments)
+    lengths = [1, 64, 200, 333, 0, 129]
+    T, H, K, V = sum(lengths), 2, 8, 6
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    q, k = rng.standard_normal((2, T, H, K))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, V))
+    g = -0.3 * rng.random((T, H, K))
+    beta = rng.random((T, H))
+    init = 0.1 * rng.standard_normal((len(lengths), H, K, V))
+    ref_o, ref_f = oracle.prefill(q, k, v, g, beta, 0.4, init, cu)
+    o, f = chunked.prefill_segmented(q, k, v, g, beta, 0.4, init, cu, chunk=16, segments=segments)
+    assert np.abs(o - ref_o).max() <= 1e-10 * np.abs(ref_o).max()
+    assert np.abs(f - ref_f).max() <= 1e-10 * np.abs(ref_f).max()
+
+
 def test_chunked_restatement_strong_gates():
     """Gates down to -5 per step: the exact-exponential chunk algebra still agrees."""
     rng = np.random.default_rng(30)
