@@ -9,7 +9,8 @@ pointers; importing the op functions raises if the library is missing.
 """
 from __future__ import annotations
 
-__all__ = ["chunk_prefill", "chunk_prefill_paged", "chunk_prefill_from_host", "recurrent_decode",
+__all__ = ["chunk_prefill", "chunk_prefill_paged", "chunk_prefill_from_host", "piece_bounds",
+           "piece_cu_seqlens", "recurrent_decode",
            "prefill_workspace", "kda_chunk_prefill", "kda_chunk_prefill_ws",
            "kda_chunk_prefill_paged_ws", "kda_chunk_prefill_noalloc",
            "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_paged", "kda_recurrent_decode",
@@ -118,6 +119,30 @@ def recurrent_decode(q, k, v, g, beta, state_pool, state_idx, scale=None, out_dt
     return out
 
 
+def piece_bounds(total_tokens: int, segments: int, chunk: int = 64):
+    """Cut the packed token range [0, total_tokens) into at most ``segments`` pieces:
+    bounds[s] .. bounds[s + 1] is piece s, every inner boundary a multiple of ``chunk``,
+    the pieces as even in chunks as the count allows.  Host logic only."""
+    T = int(total_tokens)
+    nch = (T + chunk - 1) // chunk
+    segments = max(1, min(int(segments), max(nch, 1)))
+    return [chunk * ((nch * s) // segments) for s in range(segments)] + [T]
+
+
+def piece_cu_seqlens(cu_seqlens, bounds):
+    """Per piece, the cu_seqlens of every sequence clipped to the piece and counted from
+    its first token (a sequence outside the piece has an empty range), as int32 rows
+    padded to 16 bytes.  Host logic only."""
+    import torch
+    cu = torch.as_tensor(cu_seqlens).to(torch.int64)
+    N = cu.numel() - 1
+    row = (N + 1 + 3) // 4 * 4
+    cu_seg = torch.zeros(len(bounds) - 1, row, dtype=torch.int32)
+    for s_, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
+        cu_seg[s_, :N + 1] = (cu - b0).clamp(0, b1 - b0).to(torch.int32)
+    return cu_seg
+
+
 def chunk_prefill_from_host(q, k, v, g, beta, scale=None, init_state=None, cu_seqlens=None,
                             out_dtype=None, segments: int = 4, device=None, buffers=None):
     """Chunked prefill of HOST (pinned) inputs, returning HOST outputs.
@@ -146,18 +171,11 @@ def chunk_prefill_from_host(q, k, v, g, beta, scale=None, init_state=None, cu_se
     if cu_seqlens is None:
         cu_seqlens = torch.tensor([0, T], dtype=torch.int32)
     N = cu_seqlens.numel() - 1
-    chunk = 64
-    nch = (T + chunk - 1) // chunk
-    segments = max(1, min(int(segments), nch))
-    bounds = [chunk * ((nch * s) // segments) for s in range(segments)] + [T]
+    bounds = piece_bounds(T, segments)
+    segments = len(bounds) - 1
     if buffers is None:
-        # per-piece cu_seqlens (each sequence clipped to the piece), one pinned host block
-        # whose rows are padded to 16 bytes (the C ABI wants 16-byte aligned pointers)
-        cu = cu_seqlens.to(torch.int64)
-        row = (N + 1 + 3) // 4 * 4
-        cu_seg = torch.zeros(segments, row, dtype=torch.int32)
-        for s_, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
-            cu_seg[s_, :N + 1] = (cu - b0).clamp(0, b1 - b0).to(torch.int32)
+        # per-piece cu_seqlens, rows padded to 16 bytes (the C ABI wants 16-byte aligned pointers)
+        cu_seg = piece_cu_seqlens(cu_seqlens, bounds)
         buffers = {
             "q": torch.empty(q.shape, dtype=q.dtype, device=device),
             "k": torch.empty(k.shape, dtype=k.dtype, device=device),
