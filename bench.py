@@ -223,7 +223,7 @@ def measure_prefill(args, dev, stream, flush, world):
     cu = case.cu_seqlens.to(dev)
     out = torch.empty_like(v)                       # bf16 output
     fin = torch.empty(case.N, H, K, V, dtype=torch.float32, device=dev)
-    ws = torch.empty(_native.kda_chunk_prefill_workspace_bytes(case.N, H, K, V, q.dtype),
+    ws = torch.zeros(_native.kda_chunk_prefill_workspace_bytes(case.N, H, K, V, q.dtype),
                      dtype=torch.uint8, device=dev)
 
     def step():

@@ -17,13 +17,10 @@
  *                            chunk (64 tokens), from an optional initial state;
  *                            returns the outputs and the final state per sequence
  *                            (the state carried into decode, PR #113).
- *   kda_chunk_prefill_ws  -- the same prefill with a caller workspace, through which
- *                            the four value-tile CTAs of a head share the per-chunk
- *                            operands instead of each building them (faster; same
- *                            result up to fp32 rounding).
+ *   kda_chunk_prefill_ws  -- the same prefill with a caller-owned workspace instead of
+ *                            the library's own scratch (any number of calls in flight).
  *   kda_chunk_prefill_paged -- the same prefill with the initial and final states in
- *                            paged pool slots selected per sequence (in place); its _ws
- *                            form runs on the shared-operand kernel.
+ *                            paged pool slots selected per sequence (in place).
  *   kda_recurrent_decode  -- one token per sequence against the state held in a
  *                            paged pool slot, updated in place (state slots keyed
  *                            by per-sequence indices, PR #122 block B2); its
@@ -41,10 +38,26 @@
  *    bf16 out holds exactly the fp32 result rounded to nearest).  g, beta and all
  *    states are fp32, except the bf16 pool of kda_recurrent_decode_bf16_state.  g is the NATURAL-log gate (g <= 0 for a decay); the kernels
  *    work in exp2 space internally.  Accumulation is fp32.
- *  * The caller owns every buffer.  The library allocates no device or host memory,
- *    keeps no per-call state, and synchronises nothing: all work is enqueued on
- *    `stream` (a cudaStream_t; NULL = the legacy default stream).  Errors from the
- *    kernels themselves surface at the caller's next synchronisation.
+ *  * The caller owns every buffer.  The library allocates no device or host memory
+ *    and synchronises nothing (except kda_chunk_prefill_status, which says so): all
+ *    work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *    Errors from the kernels themselves surface at the caller's next synchronisation.
+ *  * Prefill scratch.  The tensor-core prefill (bf16 q/k/v, K = V = 128) passes each
+ *    chunk's operands from the CTAs that build them to the CTA that scans the state
+ *    through a ring in device memory.  The _ws entry points take that ring from the
+ *    caller; the others use one device array inside the library (about 24 MB per device,
+ *    present from load), so on one device only ONE prefill without a workspace may be in
+ *    flight at a time: calls on one stream are ordered and safe, calls whose executions
+ *    overlap (several streams or host threads) race and give wrong results.
+ *  * Bounded waits.  The tensor-core prefill's CTAs wait on one another; every such wait
+ *    is bounded (2 s by default, kda_set_prefill_wait_limit).  A wait that runs out ends
+ *    the launch early and leaves a status in the scratch that kda_chunk_prefill_status
+ *    reports as KDA_ERR_TIMEOUT; the outputs of that launch are then incomplete.
+ *  * Range.  The tensor-core prefill rounds its operands to fp16: v, the states and the
+ *    per-chunk corrected values (about v minus the state's prediction) must stay below
+ *    65,504 in magnitude, and q and k are expected at unit scale (L2-normalised keys, as
+ *    KDA uses them).  Gates g <= 0 (decays) of any strength are covered; a growth gate
+ *    (g > 0) is covered while the state stays in that range.
  *  * Return value: KDA_OK (0) or a negative kda_status; on error nothing has been
  *    enqueued.  kda_status_string() names a status.
  *  * Aliasing: no output may overlap an input byte range, except that the prefill's
@@ -63,7 +76,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 3
+#define KDA_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define KDA_API __attribute__((visibility("default")))
@@ -83,7 +96,9 @@ enum kda_status {
                                    non-finite scale */
     KDA_ERR_UNSUPPORTED = -2,   /* K or V outside {64, 128}, unknown dtype or out_dtype */
     KDA_ERR_ALIAS = -3,         /* an output overlaps an input */
-    KDA_ERR_CUDA = -4           /* a CUDA runtime call or launch failed (see kda_last_cuda_error) */
+    KDA_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed (see kda_last_cuda_error) */
+    KDA_ERR_TIMEOUT = -5        /* a bounded wait inside the prefill kernel ran out (reported by
+                                   kda_chunk_prefill_status) */
 };
 
 /* KDA_ABI_VERSION of the loaded library. */
@@ -126,6 +141,12 @@ KDA_API int kda_last_cuda_error(void);
  *                                                 empty one), or NULL to skip.  May be
  *                                                 exactly init_state.
  *   total_tokens, num_seqs >= 0; H >= 1; K, V in {64, 128}; dtype, out_dtype kda_dtypes.
+ *
+ * bf16 q/k/v with K = V = 128 run on the tensor-core kernel with the library's scratch
+ * (one such call in flight per device, see "Prefill scratch"; KDA_ERR_UNSUPPORTED if
+ * num_seqs * H would need more than it holds, which it never does: the ring is sized by
+ * at most 40 scanners whatever the batch); other shapes and fp32 inputs on an exact
+ * CUDA-core kernel that needs no scratch.
  */
 KDA_API int kda_chunk_prefill(const void *q, const void *k, const void *v,
                               const float *g, const float *beta, float scale,
@@ -136,11 +157,10 @@ KDA_API int kda_chunk_prefill(const void *q, const void *k, const void *v,
                               int32_t out_dtype, void *stream);
 
 /*
- * Bytes of workspace kda_chunk_prefill_ws needs for these sizes on the CURRENT device
- * (the ring of per-chunk operand records of the clusters that can be resident at
- * once: at most (SMs / 4) x 8 x 66,816 bytes, ~20 MB on a 152-SM GPU, whatever
- * num_seqs is).  0 when the call needs none: num_seqs == 0, or shapes that do not run
- * on the shared-operand kernel (dtype fp32, or K or V != 128).
+ * Bytes of workspace kda_chunk_prefill_ws needs for these sizes: the record ring of
+ * min(num_seqs * H, 40) scanners, 8 records of 74,752 bytes each, plus 2.9 KB of flags
+ * (at most 23.9 MB).  0 when the call needs none: num_seqs == 0, or shapes that do not
+ * run on the tensor-core kernel (dtype fp32, or K or V != 128).
  */
 KDA_API size_t kda_chunk_prefill_workspace_bytes(int32_t num_seqs, int32_t num_heads,
                                                  int32_t head_dim_k, int32_t head_dim_v,
@@ -150,19 +170,18 @@ KDA_API size_t kda_chunk_prefill_workspace_bytes(int32_t num_seqs, int32_t num_h
  * kda_chunk_prefill with a caller-owned device workspace.
  *
  * Same operation, arguments, conventions and results as kda_chunk_prefill (vllm.cpp PR
- * #110, commit description; PR #113, commit body); only the schedule differs: the four
- * CTAs that hold the 32-column value tiles of one (sequence, head) form a thread-block
- * cluster, each builds the intra-chunk operands (gate cumsum, decayed factors, A_kk,
- * A_qk and the triangular inverse) of every fourth chunk, and all four read them back
- * through a ring in `workspace`.  Outputs agree with kda_chunk_prefill up to fp32
- * summation order.
+ * #110, commit description; PR #113, commit body), on the same kernel; only the ring
+ * that carries each chunk's operands from the CTAs that build them (gate cumsum, decayed
+ * factors, A_kk, A_qk, the triangular inverse, W and U) to the CTA that scans the state
+ * is the caller's.
  *
- *   workspace        device pointer, 16-byte aligned, at least
+ *   workspace        device memory of the CURRENT device, 16-byte aligned, at least
  *                    kda_chunk_prefill_workspace_bytes(num_seqs, num_heads, head_dim_k,
- *                    head_dim_v, dtype) bytes (queried on the device that runs the call);
- *                    may be NULL when that is 0.  Contents need no initialisation and
- *                    are garbage afterwards.  It must not overlap any other argument
- *                    (KDA_ERR_ALIAS), and two calls in flight at once need two workspaces.
+ *                    head_dim_v, dtype) bytes; may be NULL when that is 0.  It must be
+ *                    ZERO-FILLED before its first use (cudaMemset); the kernel leaves it
+ *                    reusable, so later calls need no clearing.  It must not overlap any
+ *                    other argument (KDA_ERR_ALIAS), and two calls in flight at once need
+ *                    two workspaces.  Host or another device's memory: KDA_ERR_INVALID_ARG.
  *   workspace_bytes  its size; smaller than required -> KDA_ERR_INVALID_ARG.
  * Every other argument as for kda_chunk_prefill.
  */
@@ -176,21 +195,19 @@ KDA_API int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
                                  void *stream);
 
 /*
- * kda_chunk_prefill_ws without a caller workspace: the record ring lives in a
- * file-scope device array of the library (48 clusters x 8 x 66,816 bytes = 25.7 MB per
- * device, there from the moment the library is loaded).  The pages have no counterpart
- * of this entry point; it exists for callers that cannot pass a workspace across the
- * C ABI.
+ * kda_chunk_prefill for callers that cannot allocate device memory.  The pages have no
+ * counterpart of this entry point: it serves hosts whose allocator is not reachable
+ * through the C ABI (a runtime that owns the device heap, a plug-in loaded into another
+ * program), which can pass inputs and outputs but no workspace.  The scratch is the
+ * library's own file-scope device array (24 MB per device, zero at load, present from
+ * load until exit); the address is looked up on each call with cudaGetSymbolAddress,
+ * and no call allocates or frees anything.
  *
- * Arguments, results and errors as for kda_chunk_prefill_ws, plus:
- *   KDA_ERR_UNSUPPORTED  the device can keep more clusters resident than the array has
- *                        room for (more than 48, i.e. more than 192 SMs).
- * Every call on a device uses the SAME array: two calls whose executions overlap (on
- * different streams, or from different host threads without ordering) race on it and
- * give wrong results; calls enqueued on one stream are ordered and safe.  The array
- * needs no initialisation.  The first call on each device looks up the array's
- * address and queries the resident-cluster count, so make it before capturing the
- * stream into a CUDA graph.
+ * Arguments, results and errors as for kda_chunk_prefill (which uses the same array).
+ * Every call on a device uses the SAME array, which keeps the last call's contents:
+ * two calls whose executions overlap (on different streams, or from different host
+ * threads without ordering) race on it and give wrong results; calls enqueued on one
+ * stream are ordered and safe.
  */
 KDA_API int kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
                                       const float *g, const float *beta, float scale,
@@ -199,6 +216,28 @@ KDA_API int kda_chunk_prefill_noalloc(const void *q, const void *k, const void *
                                       int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
                                       int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
                                       int32_t out_dtype, void *stream);
+
+/*
+ * Device status of the last tensor-core prefill that used `workspace` (NULL: the
+ * library's scratch on the current device), after `stream` has finished.
+ *
+ * SYNCHRONISES `stream`, reads the status word the kernel leaves in the scratch and
+ * clears it.  KDA_OK: no wait ran out; KDA_ERR_TIMEOUT: a bounded wait inside the kernel
+ * ran out (its CTAs abandoned the launch, drained their own copies and MMAs and exited;
+ * outputs and final states of that launch are incomplete); KDA_ERR_CUDA: the stream
+ * reported an error or the read failed.  This is the failure report of the bounded
+ * waits that the prefill's CTAs use to hand chunks to one another; there is no
+ * counterpart on the pages.
+ */
+KDA_API int kda_chunk_prefill_status(const void *workspace, void *stream);
+
+/*
+ * Limit, in nanoseconds, of every wait inside the tensor-core prefill kernels launched
+ * after this call (process-wide; 0 restores the default of 2 s).  A limit far below a
+ * chunk's build time makes the waits run out on purpose, which is how the timeout path
+ * is tested; no launch then hangs or faults.
+ */
+KDA_API void kda_set_prefill_wait_limit(uint64_t nanoseconds);
 
 /*
  * Chunked prefill whose per-sequence states live in paged pool slots.
@@ -218,6 +257,8 @@ KDA_API int kda_chunk_prefill_noalloc(const void *q, const void *k, const void *
  *                                              An index outside [0, num_slots) reads and
  *                                              writes no slot: that sequence runs from a
  *                                              zero state and its final state is dropped.
+ * Runs on the library's scratch like kda_chunk_prefill (one such call in flight per
+ * device).
  */
 KDA_API int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
                                     const float *g, const float *beta, float scale,
@@ -228,10 +269,10 @@ KDA_API int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
                                     int32_t dtype, int32_t out_dtype, void *stream);
 
 /*
- * kda_chunk_prefill_paged with a caller workspace: the same operation on the
- * shared-operand cluster kernel of kda_chunk_prefill_ws (same workspace rules and size,
- * kda_chunk_prefill_workspace_bytes(num_seqs, ...)).  The workspace must not overlap
- * any other argument, the pool included (KDA_ERR_ALIAS).
+ * kda_chunk_prefill_paged with a caller workspace: the same operation with the
+ * workspace rules and size of kda_chunk_prefill_ws (kda_chunk_prefill_workspace_bytes(
+ * num_seqs, ...)).  The workspace must not overlap any other argument, the pool
+ * included (KDA_ERR_ALIAS).
  */
 KDA_API int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void *v,
                                        const float *g, const float *beta, float scale,

@@ -13,13 +13,14 @@ __all__ = ["chunk_prefill", "chunk_prefill_paged", "chunk_prefill_from_host", "p
            "piece_cu_seqlens", "recurrent_decode",
            "prefill_workspace", "kda_chunk_prefill", "kda_chunk_prefill_ws",
            "kda_chunk_prefill_paged_ws", "kda_chunk_prefill_noalloc",
-           "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_paged", "kda_recurrent_decode",
-           "kda_recurrent_decode_bf16_state"]
+           "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_paged", "kda_chunk_prefill_status",
+           "kda_set_prefill_wait_limit", "kda_recurrent_decode", "kda_recurrent_decode_bf16_state"]
 
 
 def __getattr__(name):
     if name in ("kda_chunk_prefill", "kda_chunk_prefill_ws", "kda_chunk_prefill_workspace_bytes",
                 "kda_chunk_prefill_paged", "kda_chunk_prefill_paged_ws", "kda_chunk_prefill_noalloc",
+                "kda_chunk_prefill_status", "kda_set_prefill_wait_limit",
                 "kda_recurrent_decode", "kda_recurrent_decode_bf16_state", "KdaError"):
         from . import _native
         return getattr(_native, name)
@@ -32,9 +33,9 @@ _WORKSPACES = {}
 def prefill_workspace(num_seqs, num_heads, head_dim_k, head_dim_v, dtype, device=None,
                       stream=None):
     """The device workspace ``kda_chunk_prefill_ws`` needs for these sizes (None when it
-    needs none), allocated with torch and cached per (device, stream): calls enqueued on
-    one stream run one after another and can share it; calls on different streams get
-    different buffers.  It only grows."""
+    needs none), allocated zero-filled with torch and cached per (device, stream): calls
+    enqueued on one stream run one after another and can share it; calls on different
+    streams get different buffers.  It only grows."""
     import torch
     from . import _native
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
@@ -45,7 +46,7 @@ def prefill_workspace(num_seqs, num_heads, head_dim_k, head_dim_v, dtype, device
     key = (dev.index, st.cuda_stream)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < n:
-        ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        ws = torch.zeros(n, dtype=torch.uint8, device=dev)
         _WORKSPACES[key] = ws
     return ws
 

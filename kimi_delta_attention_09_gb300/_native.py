@@ -17,14 +17,16 @@ KDA_ERR_INVALID_ARG = -1
 KDA_ERR_UNSUPPORTED = -2
 KDA_ERR_ALIAS = -3
 KDA_ERR_CUDA = -4
+KDA_ERR_TIMEOUT = -5
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
             "kda_chunk_prefill", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_ws",
             "kda_chunk_prefill_noalloc", "kda_chunk_prefill_paged_ws",
-            "kda_chunk_prefill_paged", "kda_recurrent_decode", "kda_recurrent_decode_bf16_state")
+            "kda_chunk_prefill_paged", "kda_chunk_prefill_status", "kda_set_prefill_wait_limit",
+            "kda_recurrent_decode", "kda_recurrent_decode_bf16_state")
 
 
 class KdaError(RuntimeError):
@@ -64,6 +66,10 @@ def _load() -> ctypes.CDLL:
                                                i64, i32, i32, i32, i32, i32, i32, i32, vp,
                                                ctypes.c_size_t, vp]
     lib.kda_chunk_prefill_paged_ws.restype = ctypes.c_int
+    lib.kda_chunk_prefill_status.argtypes = [vp, vp]
+    lib.kda_chunk_prefill_status.restype = ctypes.c_int
+    lib.kda_set_prefill_wait_limit.argtypes = [ctypes.c_uint64]
+    lib.kda_set_prefill_wait_limit.restype = None
     lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp,
                                          i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_recurrent_decode.restype = ctypes.c_int
@@ -149,8 +155,8 @@ def kda_chunk_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out, fina
 
 def kda_chunk_prefill_workspace_bytes(num_seqs: int, num_heads: int, head_dim_k: int,
                                       head_dim_v: int, dtype) -> int:
-    """Workspace bytes ``kda_chunk_prefill_ws`` needs on the current device (``dtype``: a
-    torch dtype of q/k/v)."""
+    """Workspace bytes ``kda_chunk_prefill_ws`` needs (``dtype``: a torch dtype of q/k/v).
+    The workspace must be zero-filled before its first use (``torch.zeros``)."""
     import torch
     code = KDA_DTYPE_BF16 if dtype == torch.bfloat16 else KDA_DTYPE_F32
     return int(lib.kda_chunk_prefill_workspace_bytes(int(num_seqs), int(num_heads), int(head_dim_k),
@@ -191,8 +197,8 @@ def kda_chunk_prefill_ws(q, k, v, g, beta, scale, init_state, cu_seqlens, out, f
 
 def kda_chunk_prefill_noalloc(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
                               stream=None) -> None:
-    """Enqueue ``kda_chunk_prefill_noalloc``: ``kda_chunk_prefill_ws`` with the library's
-    own static device scratch (one call in flight per device at a time)."""
+    """Enqueue ``kda_chunk_prefill_noalloc``: the prefill on the library's own static
+    device scratch (one call in flight per device at a time)."""
     T, H, K = q.shape
     V = v.shape[-1]
     N = cu_seqlens.numel() - 1
@@ -277,6 +283,21 @@ def kda_chunk_prefill_paged_ws(q, k, v, g, beta, scale, state_pool, state_idx, c
                                         _ptr(out), T, N, S, H, K, V, _dtype_code(q), _dtype_code(out),
                                         _ptr(workspace), ws_bytes, _stream_handle(stream))
     _check("kda_chunk_prefill_paged_ws", rc)
+
+
+def kda_chunk_prefill_status(workspace=None, stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device status of the last
+    tensor-core prefill on ``workspace`` (None: the library's scratch): ``KDA_OK`` or
+    ``KDA_ERR_TIMEOUT``.  Raises on a CUDA error."""
+    rc = lib.kda_chunk_prefill_status(_ptr(workspace), _stream_handle(stream))
+    if rc not in (KDA_OK, KDA_ERR_TIMEOUT):
+        _check("kda_chunk_prefill_status", rc)
+    return int(rc)
+
+
+def kda_set_prefill_wait_limit(nanoseconds: int) -> None:
+    """Limit of every wait inside later tensor-core prefill launches (0: the default)."""
+    lib.kda_set_prefill_wait_limit(int(nanoseconds))
 
 
 def _decode(fn, q, k, v, g, beta, scale, state_pool, state_idx, out, pool_dtype, stream):

@@ -2,7 +2,6 @@
 // alias guard and kernel selection.  No allocation, no synchronisation.
 #include <cmath>
 #include <cstdint>
-#include <mutex>
 
 #include "kda.h"
 #include "kda_internal.cuh"
@@ -39,44 +38,63 @@ int finish(cudaError_t e)
     return KDA_OK;
 }
 
-// bf16 inputs with K = V = 128 run on tensor cores; other shapes and fp32 inputs on
-// the exact CUDA-core kernel.
-int launch_prefill(const kda::PrefillArgs &a, void *stream)
+// Shapes the tensor-core kernel does not cover (fp32 inputs, K or V = 64) run on the
+// exact CUDA-core kernel, which needs no workspace.
+int launch_prefill_simt(const kda::PrefillArgs &a, void *stream)
 {
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    return finish(kda::prefill_tc_supported(a) ? kda::launch_prefill_tc(a, st)
-                                               : kda::launch_prefill_simt(a, st));
+    return finish(kda::launch_prefill_simt(a, static_cast<cudaStream_t>(stream)));
 }
 
-// Scratch of kda_chunk_prefill_noalloc: the cluster kernel's record ring for up to 48
-// clusters resident at once, in a file-scope device array (nothing is allocated; the
-// array exists once per device for the life of the loaded library).
-constexpr size_t kNoAllocClusters = 48;
-constexpr size_t kNoAllocScratchBytes = kNoAllocClusters * kda::kPrefillRrRing * kda::kPrefillRrRecordBytes;
-static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+// The library's own prefill workspace: the record ring of the largest scanner count, in a
+// file-scope device array (nothing is allocated; the array exists once per device for the
+// life of the loaded library, zero-filled at load as the kernel's flags require).  It
+// serves every prefill entry point that takes no workspace argument.
+constexpr size_t kStaticScratchBytes = kda::wy_workspace_bytes_for(kda::kWyScanMax);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kStaticScratchBytes];
 
-// Device address of the scratch on the current device, resolved once per device.
+// Device address of the scratch on the current device.  Looked up on every call (cheap
+// next to a prefill), so that a device reset, which reloads the module, cannot leave a
+// stale address behind.
 void *noalloc_scratch()
 {
-    static std::mutex mu;
-    static void *addr[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
-        g_last_cuda_error = (int)(e != cudaSuccess ? e : cudaErrorInvalidDevice);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
         return nullptr;
     }
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) {
-            g_last_cuda_error = (int)e;
-            return nullptr;
-        }
-        addr[dev] = p;
+    return p;
+}
+
+// Tensor-core prefill on the library scratch (entry points without a workspace).
+int launch_prefill_static(const kda::PrefillArgs &a, void *stream)
+{
+    if (!kda::prefill_wy_supported(a)) return launch_prefill_simt(a, stream);
+    if (kda::prefill_wy_workspace_bytes(a.num_seqs, a.num_heads) > kStaticScratchBytes)
+        return KDA_ERR_UNSUPPORTED;
+    void *ws = noalloc_scratch();
+    if (!ws) return KDA_ERR_CUDA;
+    return finish(kda::launch_prefill_wy(a, ws, static_cast<cudaStream_t>(stream)));
+}
+
+// Tensor-core prefill on a caller workspace, checked for size, alignment and overlap.
+int launch_prefill_ws(const kda::PrefillArgs &a, const Range (&ranges)[9], void *workspace,
+                      size_t workspace_bytes, void *stream)
+{
+    if (!kda::prefill_wy_supported(a)) return launch_prefill_simt(a, stream);
+    const size_t need = kda::prefill_wy_workspace_bytes(a.num_seqs, a.num_heads);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
+    const Range r_ws{workspace, (uint64_t)need};
+    for (const Range &r : ranges)
+        if (overlaps(r_ws, r)) return KDA_ERR_ALIAS;
+    cudaPointerAttributes attr;
+    int dev = -1;
+    if (cudaPointerGetAttributes(&attr, workspace) != cudaSuccess || cudaGetDevice(&dev) != cudaSuccess ||
+        attr.type != cudaMemoryTypeDevice || attr.device != dev) {
+        cudaGetLastError();
+        return KDA_ERR_INVALID_ARG;   // the workspace must be device memory of the current device
     }
-    return addr[dev];
+    return finish(kda::launch_prefill_wy(a, workspace, static_cast<cudaStream_t>(stream)));
 }
 
 // Validation shared by kda_chunk_prefill and kda_chunk_prefill_ws: fills `a` and the
@@ -193,6 +211,7 @@ const char *kda_status_string(int status)
     case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
     case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS";
     case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
     default: return "KDA_ERR_UNKNOWN";
     }
 }
@@ -213,7 +232,7 @@ int kda_chunk_prefill(const void *q, const void *k, const void *v,
                                  total_tokens, num_seqs, num_heads, head_dim_k, head_dim_v, dtype,
                                  out_dtype, a, ranges);
     if (st != KDA_OK || num_seqs == 0) return st;
-    return launch_prefill(a, stream);
+    return launch_prefill_static(a, stream);
 }
 
 size_t kda_chunk_prefill_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim_k,
@@ -223,7 +242,7 @@ size_t kda_chunk_prefill_workspace_bytes(int32_t num_seqs, int32_t num_heads, in
     kda::PrefillArgs a{};
     a.num_seqs = num_seqs; a.num_heads = num_heads; a.head_dim_k = head_dim_k;
     a.head_dim_v = head_dim_v; a.dtype = dtype;
-    return kda::prefill_rr_workspace_bytes(a);
+    return kda::prefill_wy_supported(a) ? kda::prefill_wy_workspace_bytes(num_seqs, num_heads) : 0;
 }
 
 int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
@@ -240,13 +259,7 @@ int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
                                  total_tokens, num_seqs, num_heads, head_dim_k, head_dim_v, dtype,
                                  out_dtype, a, ranges);
     if (st != KDA_OK || num_seqs == 0) return st;
-    const size_t need = kda::prefill_rr_workspace_bytes(a);
-    if (need == 0) return launch_prefill(a, stream);   // shapes without the shared-operand kernel
-    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
-    const Range r_ws{workspace, (uint64_t)need};
-    for (const Range &r : ranges)
-        if (overlaps(r_ws, r)) return KDA_ERR_ALIAS;
-    return finish(kda::launch_prefill_rr(a, workspace, static_cast<cudaStream_t>(stream)));
+    return launch_prefill_ws(a, ranges, workspace, workspace_bytes, stream);
 }
 
 int kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
@@ -263,12 +276,7 @@ int kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
                                  total_tokens, num_seqs, num_heads, head_dim_k, head_dim_v, dtype,
                                  out_dtype, a, ranges);
     if (st != KDA_OK || num_seqs == 0) return st;
-    const size_t need = kda::prefill_rr_workspace_bytes(a);
-    if (need == 0) return launch_prefill(a, stream);   // shapes without the cluster kernel
-    if (need > kNoAllocScratchBytes) return KDA_ERR_UNSUPPORTED;
-    void *ws = noalloc_scratch();
-    if (!ws) return KDA_ERR_CUDA;
-    return finish(kda::launch_prefill_rr(a, ws, static_cast<cudaStream_t>(stream)));
+    return launch_prefill_static(a, stream);
 }
 
 int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
@@ -285,7 +293,7 @@ int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
                                        out, total_tokens, num_seqs, num_slots, num_heads,
                                        head_dim_k, head_dim_v, dtype, out_dtype, a, ranges);
     if (st != KDA_OK || num_seqs == 0) return st;
-    return launch_prefill(a, stream);
+    return launch_prefill_static(a, stream);
 }
 
 int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void *v,
@@ -303,13 +311,29 @@ int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void *v,
                                        out, total_tokens, num_seqs, num_slots, num_heads,
                                        head_dim_k, head_dim_v, dtype, out_dtype, a, ranges);
     if (st != KDA_OK || num_seqs == 0) return st;
-    const size_t need = kda::prefill_rr_workspace_bytes(a);
-    if (need == 0) return launch_prefill(a, stream);   // shapes without the shared-operand kernel
-    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
-    const Range r_ws{workspace, (uint64_t)need};
-    for (const Range &r : ranges)
-        if (overlaps(r_ws, r)) return KDA_ERR_ALIAS;
-    return finish(kda::launch_prefill_rr(a, workspace, static_cast<cudaStream_t>(stream)));
+    return launch_prefill_ws(a, ranges, workspace, workspace_bytes, stream);
+}
+
+int kda_chunk_prefill_status(const void *workspace, void *stream)
+{
+    void *ws = const_cast<void *>(workspace);
+    if (!ws) ws = noalloc_scratch();
+    if (!ws) return KDA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t word = 0;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && word != 0) e = cudaMemset(ws, 0, sizeof(word));
+    if (e != cudaSuccess) {
+        g_last_cuda_error = (int)e;
+        return KDA_ERR_CUDA;
+    }
+    return word == kda::kStatusTimeout ? KDA_ERR_TIMEOUT : KDA_OK;
+}
+
+void kda_set_prefill_wait_limit(uint64_t nanoseconds)
+{
+    kda::set_prefill_wait_limit_ns((unsigned long long)nanoseconds);
 }
 
 static int recurrent_decode(const void *q, const void *k, const void *v,

@@ -52,9 +52,9 @@ def test_header_compiles_as_c(tmp_path):
 
 
 def test_status_strings(native):
-    assert native.lib.kda_abi_version() == 3
+    assert native.lib.kda_abi_version() == 4
     for code, name in [(0, "KDA_OK"), (-1, "KDA_ERR_INVALID_ARG"), (-2, "KDA_ERR_UNSUPPORTED"),
-                       (-3, "KDA_ERR_ALIAS"), (-4, "KDA_ERR_CUDA")]:
+                       (-3, "KDA_ERR_ALIAS"), (-4, "KDA_ERR_CUDA"), (-5, "KDA_ERR_TIMEOUT")]:
         assert native.status_string(code) == name
     assert native.status_string(7) == "KDA_ERR_UNKNOWN"
 
@@ -213,14 +213,16 @@ def _prefill_ws(native, ws, ws_bytes, **kw):
         a["K"], a["V"], a["dtype"], a["out_dtype"], vp(ws), ws_bytes, None)
 
 
-def test_workspace_query_is_zero_without_the_cluster_kernel(native):
+def test_workspace_query_is_zero_without_the_tensor_core_kernel(native):
     q = native.lib.kda_chunk_prefill_workspace_bytes
     assert q(2, 2, 128, 128, 0) == 0      # fp32 inputs
     assert q(2, 2, 64, 128, 1) == 0       # K = 64
     assert q(2, 2, 128, 64, 1) == 0       # V = 64
     assert q(0, 2, 128, 128, 1) == 0      # no sequences
-    n = q(2, 2, 128, 128, 1)
-    assert n > 0 and n % 66816 == 0       # whole records of the ring
+    # 4 (sequence, head) items -> 4 scanners: 1 KB of flags, then 8 records of 74,752 B each
+    assert q(2, 2, 128, 128, 1) == 1024 + 4 * 8 * 74752
+    # at most 40 scanners whatever the batch
+    assert q(4096, 32, 128, 128, 1) == q(20, 2, 128, 128, 1) == 6144 + 40 * 8 * 74752
 
 
 def test_prefill_ws_validation_and_alias(native):

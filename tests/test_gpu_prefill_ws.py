@@ -1,4 +1,5 @@
-"""kda_chunk_prefill_ws (per-chunk operands shared across a 4-CTA cluster through a
+"""kda_chunk_prefill_ws (the tensor-core prefill: builder CTAs hand each chunk's operand
+record to the scanner CTA of its (sequence, head) through a ring in the caller's
 workspace) on the GPU against the fp64 oracle, through the C ABI."""
 import numpy as np
 import pytest
@@ -13,7 +14,7 @@ pytestmark = pytest.mark.gpu
 def workspace_for(case):
     from kimi_delta_attention_09_gb300 import _native
     n = _native.kda_chunk_prefill_workspace_bytes(case.N, case.H, case.K, case.V, case.q.dtype)
-    return None if n == 0 else torch.empty(n, dtype=torch.uint8, device="cuda")
+    return None if n == 0 else torch.zeros(n, dtype=torch.uint8, device="cuda")
 
 
 def run_ws(case, init_in_place=False, final=True, out_dtype=torch.float32, workspace=None):
@@ -51,7 +52,7 @@ def test_workspace_size_query():
     from kimi_delta_attention_09_gb300 import _native
     n = _native.kda_chunk_prefill_workspace_bytes(1, 32, 128, 128, torch.bfloat16)
     assert n > 0 and n % 16 == 0
-    # bounded by the resident clusters, not by the number of sequences
+    # bounded by the largest scanner count, not by the number of sequences
     assert _native.kda_chunk_prefill_workspace_bytes(4096, 32, 128, 128, torch.bfloat16) <= 64 * n
     assert _native.kda_chunk_prefill_workspace_bytes(1, 32, 128, 128, torch.float32) == 0
     assert _native.kda_chunk_prefill_workspace_bytes(1, 32, 64, 128, torch.bfloat16) == 0
@@ -65,9 +66,9 @@ def test_ragged_varlen_with_initial_state():
     check_case(case)
 
 
-def test_more_work_items_than_clusters():
-    """80 (sequence, head) items, empty ones included: each persistent cluster walks
-    several items and the record ring wraps many times."""
+def test_more_work_items_than_scanners():
+    """80 (sequence, head) items, empty ones included: each scanner walks several items
+    and the record ring wraps many times."""
     case = inputs.prefill_case([0, 5, 64, 130, 1, 200, 0, 77, 300, 65], H=8, K=128, V=128,
                                dtype="bf16", seed=161, init_std=0.02)
     out, fin = check_case(case)
@@ -77,7 +78,7 @@ def test_more_work_items_than_clusters():
 
 def test_many_short_ragged_sequences():
     """40 and 70 sequences of ragged lengths (ties and empty ones included): each
-    persistent cluster walks several items of different lengths."""
+    scanner walks several items of different lengths."""
     rng = np.random.default_rng(165)
     for n_seqs in (40, 70):
         lens = [int(x) for x in rng.integers(0, 160, size=n_seqs)]
@@ -103,10 +104,9 @@ def test_bf16_output_is_the_rounded_fp32_output():
     assert torch.equal(f16, f32)
 
 
-def test_agrees_with_the_fused_kernel():
-    """Same algebra and precision as kda_chunk_prefill, so the two agree well inside the
-    oracle tolerance; they differ only where an fp16 operand of K^^T rounds differently
-    (built as k 2^(G_last - G) here, as (k 2^(m - G)) 2^(G_last - m) there)."""
+def test_library_scratch_entry_point_gives_the_same_bits():
+    """kda_chunk_prefill (the library's own scratch) runs the same kernel: bit-identical
+    outputs and final states."""
     from kimi_delta_attention_09_gb300 import _native
     case = inputs.prefill_case([300, 77], H=4, K=128, V=128, dtype="bf16", seed=164,
                                init_std=0.02)
@@ -117,21 +117,24 @@ def test_agrees_with_the_fused_kernel():
     _native.kda_chunk_prefill(q, k, v, g, beta, case.scale, cuda(case.init_state),
                               cuda(case.cu_seqlens), out, fin)
     torch.cuda.synchronize()
-    assert rel_err(o_ws, out.cpu().double().numpy()) <= 1e-3
-    assert rel_err(f_ws, fin.cpu().double().numpy()) <= 1e-3
+    assert torch.equal(o_ws.view(torch.int32), out.cpu().view(torch.int32))
+    assert torch.equal(f_ws.view(torch.int32), fin.cpu().view(torch.int32))
 
 
 def test_two_calls_with_one_workspace():
-    """The workspace needs no initialisation: a second call on the first call's leftovers
-    gives the identical result."""
+    """A workspace is reused without clearing: a second call (and one after a call of
+    other sizes) on the earlier calls' leftovers gives the identical result."""
     case = inputs.prefill_case([200, 9], H=3, K=128, V=128, dtype="bf16", seed=165,
                                init_std=0.02)
-    ws = workspace_for(case)
-    ws.fill_(0xFF)
+    other = inputs.prefill_case([64, 1, 500], H=3, K=128, V=128, dtype="bf16", seed=175)
+    ws = workspace_for(other)
     o1, f1 = run_ws(case, workspace=ws)
     o2, f2 = run_ws(case, workspace=ws)
-    assert torch.equal(o1.view(torch.int32), o2.view(torch.int32))
-    assert torch.equal(f1.view(torch.int32), f2.view(torch.int32))
+    run_ws(other, workspace=ws)
+    o3, f3 = run_ws(case, workspace=ws)
+    for o, f in ((o2, f2), (o3, f3)):
+        assert torch.equal(o1.view(torch.int32), o.view(torch.int32))
+        assert torch.equal(f1.view(torch.int32), f.view(torch.int32))
 
 
 def test_strong_gates():
@@ -160,7 +163,68 @@ def test_split_prefill_carries_state():
     assert rel_err(fin_b, ref_fin) <= TOL["bf16"]
 
 
-def test_shapes_without_the_cluster_kernel_need_no_workspace():
+def test_fast_and_exact_chunks_alternate_in_one_sequence():
+    """Chunks whose gate span leaves the fp16 factors' range (exact-exponential path) and
+    chunks on the fp16 fast path alternate inside one sequence; ragged tail."""
+    case = inputs.prefill_case([64 * 7 + 29], H=2, K=128, V=128, dtype="bf16", seed=176,
+                               init_std=0.02)
+    gen = torch.Generator().manual_seed(176)
+    strong = (-4.0 * torch.rand(case.g.shape, generator=gen)).float()
+    chunk = torch.arange(case.T) // 64
+    case.g = torch.where((chunk % 2 == 1)[:, None, None], strong, case.g).contiguous()
+    check_case(case)
+
+
+def test_large_state_and_value_magnitudes():
+    """Initial states of std 5 and values of std 100 (inputs far from unit scale, still
+    inside the fp16 operand range), with weak gates that keep the state long-lived."""
+    case = inputs.prefill_case([333, 64], H=2, K=128, V=128, dtype="bf16", seed=177,
+                               init_std=5.0, gate_scale=0.02)
+    case.v = (case.v.float() * 100.0).to(torch.bfloat16).contiguous()
+    check_case(case)
+
+
+def test_timeout_is_reported_and_the_context_stays_usable():
+    """A wait limit of 100 ns makes the kernel's waits run out on purpose: the launch
+    ends early, kda_chunk_prefill_status reports KDA_ERR_TIMEOUT (once), and a normal
+    launch afterwards on the same workspace is correct."""
+    from kimi_delta_attention_09_gb300 import _native
+    case = inputs.prefill_case([640, 100], H=4, K=128, V=128, dtype="bf16", seed=178,
+                               init_std=0.02)
+    ws = workspace_for(case)
+    try:
+        _native.kda_set_prefill_wait_limit(100)
+        run_ws(case, workspace=ws)
+    finally:
+        _native.kda_set_prefill_wait_limit(0)
+    assert _native.kda_chunk_prefill_status(ws) == _native.KDA_ERR_TIMEOUT
+    assert _native.kda_chunk_prefill_status(ws) == _native.KDA_OK   # read and cleared
+    check_case(case, workspace=ws)
+    assert _native.kda_chunk_prefill_status(ws) == _native.KDA_OK
+
+
+def test_workspace_must_be_device_memory_of_this_device():
+    """Pinned host memory as the workspace is refused before anything is enqueued."""
+    import ctypes
+    from kimi_delta_attention_09_gb300 import _native
+    case = inputs.prefill_case([100], H=2, K=128, V=128, dtype="bf16", seed=179)
+    q, k, v, g, beta = (cuda(x) for x in (case.q, case.k, case.v, case.g, case.beta))
+    cu = cuda(case.cu_seqlens)
+    n = _native.kda_chunk_prefill_workspace_bytes(case.N, case.H, 128, 128, torch.bfloat16)
+    host_ws = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    out = torch.zeros(v.shape, device="cuda")
+    vp = ctypes.c_void_p
+    rc = _native.lib.kda_chunk_prefill_ws(
+        vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(g.data_ptr()),
+        vp(beta.data_ptr()), case.scale, None, vp(cu.data_ptr()), vp(out.data_ptr()), None,
+        case.T, case.N, case.H, 128, 128, 1, 0, vp(host_ws.data_ptr()), n,
+        vp(torch.cuda.current_stream().cuda_stream))
+    assert rc == _native.KDA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
+
+
+def test_shapes_without_the_tensor_core_kernel_need_no_workspace():
     """fp32 inputs and K = 64 run the other kernels; workspace None is accepted."""
     for dtype, K, V in (("f32", 128, 128), ("bf16", 64, 128)):
         case = inputs.prefill_case([70, 3], H=2, K=K, V=V, dtype=dtype, seed=168, init_std=0.02)
@@ -240,7 +304,7 @@ def test_paged_ws_reads_and_writes_its_slots():
 
 def test_paged_ws_out_of_range_slot_and_many_items():
     """An index outside [0, S) reads and writes no slot (zero start, final state dropped);
-    40 sequences x 3 heads are more work items than clusters."""
+    40 sequences x 3 heads are more work items than scanners."""
     lens = [(37 * i) % 150 for i in range(40)]
     case = inputs.prefill_case(lens, H=3, K=128, V=128, dtype="bf16", seed=172)
     gen = torch.Generator().manual_seed(173)
@@ -264,7 +328,7 @@ def test_paged_ws_out_of_range_slot_and_many_items():
 
 
 def test_paged_ws_then_paged_decode():
-    """The runner's path: a prompt through the paged cluster prefill, then token-by-token
+    """The runner's path: a prompt through the paged tensor-core prefill, then token-by-token
     decode on the same slot = the oracle over the whole sequence."""
     from kimi_delta_attention_09_gb300 import _native
     T0, steps, H = 150, 5, 2

@@ -19,7 +19,7 @@ def _run(case, entry, out_dtype=torch.float32):
     fin = torch.full((case.N, case.H, case.K, case.V), float("nan"), device="cuda")
     if entry == "ws":
         n = _native.kda_chunk_prefill_workspace_bytes(case.N, case.H, case.K, case.V, case.q.dtype)
-        ws = torch.empty(n, dtype=torch.uint8, device="cuda") if n else None
+        ws = torch.zeros(n, dtype=torch.uint8, device="cuda") if n else None
         _native.kda_chunk_prefill_ws(q, k, v, g, beta, case.scale, cuda(case.init_state), cu, out,
                                      fin, ws)
     else:
