@@ -4,10 +4,11 @@
 A step is one pass of the hot path over the single-prompt workload (B=1, H=32,
 T=4096, K=V=128, bf16 q/k/v, fp32 gates/state, zero initial state, final state
 returned): one ``kda_chunk_prefill_ws`` call (the 4-CTA cluster kernel that shares each
-chunk's operands across the value tiles).  ``value`` is prefill tokens/s over all
-ranks; the same run also times the paged-decode workload (256 sequences x 1 token,
-H=32, K=V=128, 1024-slot fp32 pool, 64 steps carrying state in place) and reports
-its state GB/s under "decode".
+chunk's operands across the value tiles).  ``value`` is prefill tokens/s.  The same run
+also times the varlen packed workload (8 sequences, lengths U[256, 8192], nonzero
+initial states) under "prefill_varlen", the long prompt (T=65536) under "prefill_long",
+and the paged-decode workload (256 sequences x 1 token, H=32, K=V=128, 1024-slot fp32
+pool, 64 steps carrying state in place) under "decode" / "decode_bf16_state".
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--only all|prefill|decode] [--decode-seqs S]
@@ -18,9 +19,10 @@ smaller case; the default run measures everything.
 Timing: CUDA events on the launching stream around each step, with L2 flushed
 (a 256 MiB write) between timed steps; a short device sleep is queued ahead of each
 start event so the event pair brackets the kernel, not the host-side launch.
-N > 1 (torchrun): every rank runs its own replica of the workload (weak scaling),
-step times are max-reduced over ranks.  ``--impl reference`` times the fp64 CPU
-oracle on the host cores instead (a bounded sample of the same workload per step).
+The benchmark is single-GPU (every call of the library runs on one GPU): ``--gpus`` > 1
+or a torchrun launch with WORLD_SIZE > 1 exits with an error line.  ``--impl reference``
+times the fp64 CPU oracle on the host cores instead (a bounded sample of the same
+workload per step; under torchrun rank 0 alone runs it).
 """
 from __future__ import annotations
 
@@ -156,39 +158,6 @@ def gpu_id_for(device_index: int) -> str:
         return vis.split(",")[device_index] if vis else str(device_index)
 
 
-# ------------------------------------------------------------------ distributed
-
-def dist_setup():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch
-        import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if backend == "nccl":
-            torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
-    return rank, world, local
-
-
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64,
-                     device="cuda" if torch.cuda.is_available() else "cpu")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
 # ------------------------------------------------------------------ our arm
 
 def time_steps(fn, steps, warmup, stream, flush_buf, sleep_cycles=200_000):
@@ -212,32 +181,68 @@ def time_steps(fn, steps, warmup, stream, flush_buf, sleep_cycles=200_000):
     return times
 
 
-def measure_prefill(args, dev, stream, flush, world):
-    """Device time of kda_chunk_prefill_ws on the single-prompt workload."""
-    import torch
-    from kimi_delta_attention_09_gb300 import _native, inputs
-    case = inputs.single_prompt()
+def prefill_case_bytes(case):
+    """Algorithmic HBM bytes of one prefill call: the per-(token, head) traffic plus the
+    final states written and, when given, the initial states read (64 KiB each)."""
     T, H, K, V = case.T, case.H, case.K, case.V
+    b = T * H * prefill_bytes_per_token_head() + case.N * H * K * V * 4
+    if case.init_state is not None:
+        b += case.N * H * K * V * 4
+    return b
+
+
+def time_prefill_case(args, case, dev, stream, flush, steps):
+    """Device times of kda_chunk_prefill_ws (the cluster kernel) on one workload."""
+    import torch
+    from kimi_delta_attention_09_gb300 import _native
+    H, K, V = case.H, case.K, case.V
     q, k, v = (x.to(dev) for x in (case.q, case.k, case.v))
     g, beta = case.g.to(dev), case.beta.to(dev)
     cu = case.cu_seqlens.to(dev)
+    init = None if case.init_state is None else case.init_state.to(dev)
     out = torch.empty_like(v)                       # bf16 output
     fin = torch.empty(case.N, H, K, V, dtype=torch.float32, device=dev)
     ws = torch.zeros(_native.kda_chunk_prefill_workspace_bytes(case.N, H, K, V, q.dtype),
                      dtype=torch.uint8, device=dev)
 
     def step():
-        _native.kda_chunk_prefill_ws(q, k, v, g, beta, case.scale, None, cu, out, fin, ws, stream)
+        _native.kda_chunk_prefill_ws(q, k, v, g, beta, case.scale, init, cu, out, fin, ws, stream)
 
-    barrier(world)
-    with ClockSampler(gpu_id_for(dev.index)) as clk:
-        times = time_steps(step, args.steps, args.warmup, stream, flush)
+    times = time_steps(step, steps, args.warmup, stream, flush)
     torch.cuda.synchronize()
-    barrier(world)
-    return case, times, clk.summary(), (q, k, v, g, beta, cu, out, fin)
+    status = _native.kda_chunk_prefill_status(ws, stream)
+    if status != _native.KDA_OK:
+        raise RuntimeError(f"prefill on {case.name} reported device status {status}")
+    return times, (q, k, v, g, beta, cu, out, fin)
 
 
-def measure_e2e(args, case, bufs, stream, flush, world):
+def measure_prefill(args, dev, stream, flush):
+    """Device time of kda_chunk_prefill_ws on the single-prompt workload."""
+    from kimi_delta_attention_09_gb300 import inputs
+    case = inputs.single_prompt()
+    with ClockSampler(gpu_id_for(dev.index)) as clk:
+        times, bufs = time_prefill_case(args, case, dev, stream, flush, args.steps)
+    return case, times, clk.summary(), bufs
+
+
+def prefill_block(case, times, peak_hbm, traffic_key, traffic, sample):
+    """The JSON block of one timed prefill workload."""
+    p_ms = statistics.mean(times)
+    p_bytes = prefill_case_bytes(case)
+    p_flops = case.T * case.H * prefill_flops_per_token_head()
+    p_gbs = p_bytes / (p_ms * 1e-3) / 1e9
+    return {"workload": case.name, "sequences": case.N, "tokens": case.T,
+            "ms_per_step": round(p_ms, 5), "ms_min": round(min(times), 5), "steps": len(times),
+            "tokens_per_s": round(case.T / (p_ms * 1e-3), 1),
+            "tflops_algorithmic": round(p_flops / (p_ms * 1e-3) / 1e12, 3),
+            "algorithmic_bytes": p_bytes, "algorithmic_flops": p_flops,
+            "roofline": {"bound": "hbm", "kernel": "kda_prefill_rr_kernel",
+                         "achieved": round(p_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                         "frac": round(p_gbs / peak_hbm, 4), "traffic": traffic.get(traffic_key)},
+            "cpu_baseline": sample}
+
+
+def measure_e2e(args, case, bufs, stream, flush):
     """The same prefill through the public host-to-host call (chunk_prefill_from_host):
     pinned host inputs in, pinned host output and final state out, every H2D and D2H
     copy inside the timed region (overlapped with the kernels piece by piece).  The
@@ -265,7 +270,7 @@ def measure_e2e(args, case, bufs, stream, flush, world):
     return times, h2d, d2h, n * segments   # one prefill kernel per piece
 
 
-def measure_decode(args, dev, stream, flush, world, bf16_state=False):
+def measure_decode(args, dev, stream, flush, bf16_state=False):
     """Device time per step of kda_recurrent_decode on the paged-decode workload
     (64 steps carrying the state in place through a 1024-slot fp32 pool); with
     bf16_state, of kda_recurrent_decode_bf16_state on the same pool stored in bf16."""
@@ -289,10 +294,8 @@ def measure_decode(args, dev, stream, flush, world, bf16_state=False):
         counter[0] += 1
         fn(sq, sk, sv, sg, sb, dcase.scale, pool, idx, dout, stream)
 
-    barrier(world)
     times = time_steps(step, DECODE_STEPS if args.only != "decode" else max(args.steps, 1),
                        args.warmup, stream, flush)
-    barrier(world)
     d_bytes = N * H * decode_bytes_per_seq_head(state_es=2 if bf16_state else 4)
     name = dcase.name if N == dcase.N else dcase.name.replace("N256", f"N{N}")
     if bf16_state:
@@ -300,10 +303,10 @@ def measure_decode(args, dev, stream, flush, world, bf16_state=False):
     return name, N, times, d_bytes
 
 
-def run_ours(args, rank, world, local):
+def run_ours(args):
     import torch
 
-    dev = torch.device("cuda", local)
+    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     peaks = load_peaks()
@@ -311,27 +314,28 @@ def run_ours(args, rank, world, local):
     traffic = load_traffic()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     line = {"metric": "KDA prefill tokens/s + TFLOP/s; decode state GB/s (fraction of roofline)",
-            "value": None, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "value": None, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
     launches = 0
 
     if args.only in ("all", "prefill"):
-        case, ptimes, clocks, bufs = measure_prefill(args, dev, stream, flush, world)
+        case, ptimes, clocks, bufs = measure_prefill(args, dev, stream, flush)
         T, H, K, V = case.T, case.H, case.K, case.V
         p_ms = statistics.mean(ptimes)
-        p_ms_max = max_over_ranks(p_ms, world)
-        p_bytes = T * H * prefill_bytes_per_token_head() + case.N * H * K * V * 4
+        p_bytes = prefill_case_bytes(case)
         p_flops = T * H * prefill_flops_per_token_head()
         p_gbs = p_bytes / (p_ms * 1e-3) / 1e9
         launches += args.steps
         line.update({
-            "value": round(world * T / (p_ms_max * 1e-3), 1),
-            "ms_per_step": round(p_ms_max, 5),
-            "config": {"workload": case.name, "global_batch": world, "seq_len": T, "heads": H,
+            "value": round(T / (p_ms * 1e-3), 1),
+            "ms_per_step": round(p_ms, 5),
+            "config": {"workload": case.name, "global_batch": 1, "seq_len": T, "heads": H,
                        "head_dim_k": K, "head_dim_v": V, "chunk": CHUNK, "out_dtype": "bf16",
-                       "parallelism": f"replicas{world}",
-                       "l2": "flushed between timed steps (256 MiB write)"},
+                       "parallelism": "one GPU",
+                       "l2": "flushed between timed steps (256 MiB write)",
+                       "also_timed": ["varlen_packed (prefill_varlen)", "long_prefill (prefill_long)",
+                                      "paged_decode (decode, decode_bf16_state)"]},
             "prefill": {"tokens_per_s": round(T / (p_ms * 1e-3), 1),
                         "tflops_algorithmic": round(p_flops / (p_ms * 1e-3) / 1e12, 3),
                         "gb_per_s_algorithmic": round(p_gbs, 1),
@@ -344,60 +348,70 @@ def run_ours(args, rank, world, local):
             "clocks": clocks,
         })
         if args.only == "all":
-            etimes, h2d, d2h, n_e2e = measure_e2e(args, case, bufs, stream, flush, world)
-            e_ms = max_over_ranks(statistics.mean(etimes), world)
+            etimes, h2d, d2h, n_e2e = measure_e2e(args, case, bufs, stream, flush)
+            e_ms = statistics.mean(etimes)
             launches += n_e2e
-            line["e2e"] = {"value": round(world * T / (e_ms * 1e-3), 1), "unit": "tokens/s",
+            line["e2e"] = {"value": round(T / (e_ms * 1e-3), 1), "unit": "tokens/s",
                            "ms_per_step": round(e_ms, 4),
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            if not args.no_cpu_baseline:
                 line["cpu_baseline"] = cpu_oracle_baseline(case, n_tokens=T)
         del bufs
+        if args.only == "all":
+            from kimi_delta_attention_09_gb300 import inputs
+            for key, make, tkey in (("prefill_varlen", inputs.varlen_packed, "prefill_rr_varlen_packed"),
+                                    ("prefill_long", inputs.long_prefill, "prefill_rr_long_prefill")):
+                c = make()
+                n = max(3, min(args.steps, 10))
+                ctimes, cbufs = time_prefill_case(args, c, dev, stream, flush, n)
+                del cbufs
+                launches += n
+                sample = None if args.no_cpu_baseline else cpu_oracle_baseline(c, n_tokens=1024, budget_s=5.0)
+                line[key] = prefill_block(c, ctimes, peak_hbm, tkey, traffic, sample)
+                del c
 
     if args.only in ("all", "decode"):
-        name, N, dtimes, d_bytes = measure_decode(args, dev, stream, flush, world)
+        name, N, dtimes, d_bytes = measure_decode(args, dev, stream, flush)
         d_ms = statistics.mean(dtimes)
-        d_ms_max = max_over_ranks(d_ms, world)
         d_gbs = d_bytes / (d_ms * 1e-3) / 1e9
         launches += len(dtimes)
         line["decode"] = {
             "workload": name, "metric": "state GB/s",
-            "value": round(world * d_bytes / (d_ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "ms_per_step": round(d_ms_max, 5), "steps": len(dtimes),
+            "value": round(d_gbs, 1), "unit": "GB/s",
+            "ms_per_step": round(d_ms, 5), "steps": len(dtimes),
             "algorithmic_bytes_per_step": d_bytes,
             "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel", "achieved": round(d_gbs, 1),
                          "peak": peak_hbm, "unit": "GB/s", "frac": round(d_gbs / peak_hbm, 4),
                          "traffic": traffic.get("decode_paged")}}
-        name, N, dtimes, d_bytes = measure_decode(args, dev, stream, flush, world, bf16_state=True)
+        name, N, dtimes, d_bytes = measure_decode(args, dev, stream, flush, bf16_state=True)
         d_ms = statistics.mean(dtimes)
-        d_ms_max = max_over_ranks(d_ms, world)
         d_gbs = d_bytes / (d_ms * 1e-3) / 1e9
         launches += len(dtimes)
         line["decode_bf16_state"] = {
             "workload": name, "metric": "state GB/s",
-            "value": round(world * d_bytes / (d_ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
-            "ms_per_step": round(d_ms_max, 5), "steps": len(dtimes),
+            "value": round(d_gbs, 1), "unit": "GB/s",
+            "ms_per_step": round(d_ms, 5), "steps": len(dtimes),
             "algorithmic_bytes_per_step": d_bytes,
             "roofline": {"bound": "hbm", "kernel": "kda_decode_kernel (bf16 state)",
                          "achieved": round(d_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                          "frac": round(d_gbs / peak_hbm, 4),
                          "traffic": traffic.get("decode_bf16_state_paged")}}
     line["gpu_launches"] = launches
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ oracle arm
 
-def cpu_oracle_baseline(case, n_tokens):
-    """The fp64 oracle (as it stands) on the first n_tokens of the workload."""
+def cpu_oracle_baseline(case, n_tokens, budget_s=15.0):
+    """The fp64 oracle (as it stands) on the first n_tokens of the workload (of its first
+    sequence), repeated until it has taken about `budget_s` CPU-seconds."""
     import oracle
+    n_tokens = min(n_tokens, int(case.cu_seqlens[1]))
     sl = slice(0, n_tokens)
     threads = oracle.default_threads()
     used = min(threads, case.H)
-    # repeat the sample until it has taken ~15 CPU-seconds on the threads in use
     reps, dt = 0, 0.0
-    while reps == 0 or dt * used < 15.0:
+    while reps == 0 or dt * used < budget_s:
         t0 = time.perf_counter()
         oracle.prefill(case.q[sl], case.k[sl], case.v[sl], case.g[sl], case.beta[sl], case.scale,
                        None, [0, n_tokens], nthreads=threads)
@@ -467,12 +481,16 @@ def main():
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
         return
-    rank, world, local = dist_setup()
-    run_ours(args, rank, world, local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-        dist.destroy_process_group()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1 or args.gpus > 1:
+        # every call of this library runs on one GPU (the prefill kernel's record hand-off
+        # uses a cluster multicast load, kept to single-GPU runs), so there is no multi-GPU
+        # step to time
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps({"error": "single-GPU benchmark: run with --gpus 1 and no torchrun",
+                              "n_gpus": max(world, args.gpus)}), flush=True)
+        sys.exit(2)
+    run_ours(args)
 
 
 if __name__ == "__main__":

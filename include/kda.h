@@ -42,22 +42,26 @@
  *    and synchronises nothing (except kda_chunk_prefill_status, which says so): all
  *    work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
  *    Errors from the kernels themselves surface at the caller's next synchronisation.
- *  * Prefill scratch.  The tensor-core prefill (bf16 q/k/v, K = V = 128) passes each
- *    chunk's operands from the CTAs that build them to the CTA that scans the state
- *    through a ring in device memory.  The _ws entry points take that ring from the
- *    caller; the others use one device array inside the library (about 24 MB per device,
- *    present from load), so on one device only ONE prefill without a workspace may be in
- *    flight at a time: calls on one stream are ordered and safe, calls whose executions
- *    overlap (several streams or host threads) race and give wrong results.
- *  * Bounded waits.  The tensor-core prefill's CTAs wait on one another; every such wait
- *    is bounded (2 s by default, kda_set_prefill_wait_limit).  A wait that runs out ends
- *    the launch early and leaves a status in the scratch that kda_chunk_prefill_status
- *    reports as KDA_ERR_TIMEOUT; the outputs of that launch are then incomplete.
- *  * Range.  The tensor-core prefill rounds its operands to fp16: v, the states and the
- *    per-chunk corrected values (about v minus the state's prediction) must stay below
- *    65,504 in magnitude, and q and k are expected at unit scale (L2-normalised keys, as
- *    KDA uses them).  Gates g <= 0 (decays) of any strength are covered; a growth gate
- *    (g > 0) is covered while the state stays in that range.
+ *  * Prefill scratch.  The tensor-core prefill (bf16 q/k/v, K = V = 128) runs one
+ *    4-CTA thread-block cluster per (sequence, head); each CTA builds every fourth
+ *    chunk's operands (gate cumsum, decayed factors, A_kk, A_qk, the triangular inverse)
+ *    and all four read them back through a ring of records in device memory.  The _ws
+ *    entry points take that ring from the caller; the others use one device array inside
+ *    the library (25.7 MB per device, present from load), so on one device only ONE
+ *    prefill without a workspace may be in flight at a time: calls on one stream are
+ *    ordered and safe, calls whose executions overlap (several streams or host threads)
+ *    race and give wrong results.  Every call runs on one GPU, and a ring must be device
+ *    memory of the GPU that runs the call.
+ *  * Bounded waits.  The CTAs of a cluster wait on one another and on their tensor-core
+ *    work; every such wait is bounded in time (2 s by default, kda_set_prefill_wait_limit).
+ *    A wait that runs out ends that cluster's work early and leaves a status word in the
+ *    ring's header that kda_chunk_prefill_status reports as KDA_ERR_TIMEOUT; the outputs
+ *    and final states of that launch are then incomplete.
+ *  * Range.  The tensor-core prefill rounds its operands to fp16: v, the states scaled by
+ *    2^m (m <= 0 for decays) and the per-chunk corrected values (about v minus the
+ *    state's prediction) must stay below 65,504 in magnitude, and q and k are expected at
+ *    unit scale (L2-normalised keys, as KDA uses them).  Gates of any strength are
+ *    covered (a chunk whose gate spans more than 2^16 takes an exact-exponential path).
  *  * Return value: KDA_OK (0) or a negative kda_status; on error nothing has been
  *    enqueued.  kda_status_string() names a status.
  *  * Aliasing: no output may overlap an input byte range, except that the prefill's
@@ -142,11 +146,10 @@ KDA_API int kda_last_cuda_error(void);
  *                                                 exactly init_state.
  *   total_tokens, num_seqs >= 0; H >= 1; K, V in {64, 128}; dtype, out_dtype kda_dtypes.
  *
- * bf16 q/k/v with K = V = 128 run on the tensor-core kernel with the library's scratch
- * (one such call in flight per device, see "Prefill scratch"; KDA_ERR_UNSUPPORTED if
- * num_seqs * H would need more than it holds, which it never does: the ring is sized by
- * at most 40 scanners whatever the batch); other shapes and fp32 inputs on an exact
- * CUDA-core kernel that needs no scratch.
+ * bf16 q/k/v with K = V = 128 run on the tensor-core cluster kernel with the library's
+ * scratch (one such call in flight per device, see "Prefill scratch"; any batch size: the
+ * clusters are persistent and walk the (sequence, head) work items); other shapes and
+ * fp32 inputs on an exact CUDA-core kernel that needs no scratch.
  */
 KDA_API int kda_chunk_prefill(const void *q, const void *k, const void *v,
                               const float *g, const float *beta, float scale,
@@ -157,10 +160,11 @@ KDA_API int kda_chunk_prefill(const void *q, const void *k, const void *v,
                               int32_t out_dtype, void *stream);
 
 /*
- * Bytes of workspace kda_chunk_prefill_ws needs for these sizes: the record ring of
- * min(num_seqs * H, 40) scanners, 8 records of 74,752 bytes each, plus 2.9 KB of flags
- * (at most 23.9 MB).  0 when the call needs none: num_seqs == 0, or shapes that do not
- * run on the tensor-core kernel (dtype fp32, or K or V != 128).
+ * Bytes of workspace kda_chunk_prefill_ws needs for these sizes on the CURRENT device:
+ * a 256-byte header (the device status word) and a ring of 8 records of 66,816 bytes for
+ * each of min(num_seqs * H, clusters the device keeps resident) clusters (~20 MB on a
+ * 152-SM GPU whatever num_seqs is).  0 when the call needs none: num_seqs == 0, or
+ * shapes that do not run on the tensor-core kernel (dtype fp32, or K or V != 128).
  */
 KDA_API size_t kda_chunk_prefill_workspace_bytes(int32_t num_seqs, int32_t num_heads,
                                                  int32_t head_dim_k, int32_t head_dim_v,
@@ -171,17 +175,17 @@ KDA_API size_t kda_chunk_prefill_workspace_bytes(int32_t num_seqs, int32_t num_h
  *
  * Same operation, arguments, conventions and results as kda_chunk_prefill (vllm.cpp PR
  * #110, commit description; PR #113, commit body), on the same kernel; only the ring
- * that carries each chunk's operands from the CTAs that build them (gate cumsum, decayed
- * factors, A_kk, A_qk, the triangular inverse, W and U) to the CTA that scans the state
- * is the caller's.
+ * through which the four CTAs of a cluster share each chunk's operands is the caller's.
  *
  *   workspace        device memory of the CURRENT device, 16-byte aligned, at least
  *                    kda_chunk_prefill_workspace_bytes(num_seqs, num_heads, head_dim_k,
  *                    head_dim_v, dtype) bytes; may be NULL when that is 0.  It must be
- *                    ZERO-FILLED before its first use (cudaMemset); the kernel leaves it
- *                    reusable, so later calls need no clearing.  It must not overlap any
- *                    other argument (KDA_ERR_ALIAS), and two calls in flight at once need
- *                    two workspaces.  Host or another device's memory: KDA_ERR_INVALID_ARG.
+ *                    ZERO-FILLED before its first use (cudaMemset): its header holds the
+ *                    device status word, which the kernel only sets and
+ *                    kda_chunk_prefill_status reads and clears; the rest needs no
+ *                    initialisation.  It must not overlap any other argument
+ *                    (KDA_ERR_ALIAS), and two calls in flight at once need two
+ *                    workspaces.  Host or another device's memory: KDA_ERR_INVALID_ARG.
  *   workspace_bytes  its size; smaller than required -> KDA_ERR_INVALID_ARG.
  * Every other argument as for kda_chunk_prefill.
  */
@@ -199,9 +203,9 @@ KDA_API int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
  * counterpart of this entry point: it serves hosts whose allocator is not reachable
  * through the C ABI (a runtime that owns the device heap, a plug-in loaded into another
  * program), which can pass inputs and outputs but no workspace.  The scratch is the
- * library's own file-scope device array (24 MB per device, zero at load, present from
- * load until exit); the address is looked up on each call with cudaGetSymbolAddress,
- * and no call allocates or frees anything.
+ * library's own file-scope device array (25.7 MB per device: the status header and a ring
+ * for 48 clusters; zero at load, present from load until exit); the address is looked up
+ * on each call with cudaGetSymbolAddress, and no call allocates or frees anything.
  *
  * Arguments, results and errors as for kda_chunk_prefill (which uses the same array).
  * Every call on a device uses the SAME array, which keeps the last call's contents:
@@ -223,10 +227,10 @@ KDA_API int kda_chunk_prefill_noalloc(const void *q, const void *k, const void *
  *
  * SYNCHRONISES `stream`, reads the status word the kernel leaves in the scratch and
  * clears it.  KDA_OK: no wait ran out; KDA_ERR_TIMEOUT: a bounded wait inside the kernel
- * ran out (its CTAs abandoned the launch, drained their own copies and MMAs and exited;
- * outputs and final states of that launch are incomplete); KDA_ERR_CUDA: the stream
- * reported an error or the read failed.  This is the failure report of the bounded
- * waits that the prefill's CTAs use to hand chunks to one another; there is no
+ * ran out (the clusters concerned abandoned their work, drained their own copies and
+ * MMAs and exited; outputs and final states of that launch are incomplete); KDA_ERR_CUDA:
+ * the stream reported an error or the read failed.  This is the failure report of the
+ * bounded waits that the prefill's CTAs use to hand chunks to one another; there is no
  * counterpart on the pages.
  */
 KDA_API int kda_chunk_prefill_status(const void *workspace, void *stream);

@@ -45,11 +45,14 @@ int launch_prefill_simt(const kda::PrefillArgs &a, void *stream)
     return finish(kda::launch_prefill_simt(a, static_cast<cudaStream_t>(stream)));
 }
 
-// The library's own prefill workspace: the record ring of the largest scanner count, in a
-// file-scope device array (nothing is allocated; the array exists once per device for the
-// life of the loaded library, zero-filled at load as the kernel's flags require).  It
-// serves every prefill entry point that takes no workspace argument.
-constexpr size_t kStaticScratchBytes = kda::wy_workspace_bytes_for(kda::kWyScanMax);
+// The library's own prefill workspace: the status header and a record ring for 48
+// clusters, in a file-scope device array (nothing is allocated; the array exists once per
+// device for the life of the loaded library).  It serves every prefill entry point that
+// takes no workspace argument; a device that can keep more than 48 clusters resident runs
+// 48 (the clusters are persistent and walk the work items).
+constexpr size_t kStaticClusters = 48;
+constexpr size_t kStaticScratchBytes =
+    kda::kPrefillRrHeaderBytes + kStaticClusters * kda::kPrefillRrRing * kda::kPrefillRrRecordBytes;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kStaticScratchBytes];
 
 // Device address of the scratch on the current device.  Looked up on every call (cheap
@@ -69,20 +72,18 @@ void *noalloc_scratch()
 // Tensor-core prefill on the library scratch (entry points without a workspace).
 int launch_prefill_static(const kda::PrefillArgs &a, void *stream)
 {
-    if (!kda::prefill_wy_supported(a)) return launch_prefill_simt(a, stream);
-    if (kda::prefill_wy_workspace_bytes(a.num_seqs, a.num_heads) > kStaticScratchBytes)
-        return KDA_ERR_UNSUPPORTED;
+    if (!kda::prefill_rr_supported(a)) return launch_prefill_simt(a, stream);
     void *ws = noalloc_scratch();
     if (!ws) return KDA_ERR_CUDA;
-    return finish(kda::launch_prefill_wy(a, ws, static_cast<cudaStream_t>(stream)));
+    return finish(kda::launch_prefill_rr(a, ws, kStaticScratchBytes, static_cast<cudaStream_t>(stream)));
 }
 
 // Tensor-core prefill on a caller workspace, checked for size, alignment and overlap.
 int launch_prefill_ws(const kda::PrefillArgs &a, const Range (&ranges)[9], void *workspace,
                       size_t workspace_bytes, void *stream)
 {
-    if (!kda::prefill_wy_supported(a)) return launch_prefill_simt(a, stream);
-    const size_t need = kda::prefill_wy_workspace_bytes(a.num_seqs, a.num_heads);
+    if (!kda::prefill_rr_supported(a)) return launch_prefill_simt(a, stream);
+    const size_t need = kda::prefill_rr_workspace_bytes(a);
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return KDA_ERR_INVALID_ARG;
     const Range r_ws{workspace, (uint64_t)need};
     for (const Range &r : ranges)
@@ -94,7 +95,7 @@ int launch_prefill_ws(const kda::PrefillArgs &a, const Range (&ranges)[9], void 
         cudaGetLastError();
         return KDA_ERR_INVALID_ARG;   // the workspace must be device memory of the current device
     }
-    return finish(kda::launch_prefill_wy(a, workspace, static_cast<cudaStream_t>(stream)));
+    return finish(kda::launch_prefill_rr(a, workspace, need, static_cast<cudaStream_t>(stream)));
 }
 
 // Validation shared by kda_chunk_prefill and kda_chunk_prefill_ws: fills `a` and the
@@ -242,7 +243,7 @@ size_t kda_chunk_prefill_workspace_bytes(int32_t num_seqs, int32_t num_heads, in
     kda::PrefillArgs a{};
     a.num_seqs = num_seqs; a.num_heads = num_heads; a.head_dim_k = head_dim_k;
     a.head_dim_v = head_dim_v; a.dtype = dtype;
-    return kda::prefill_wy_supported(a) ? kda::prefill_wy_workspace_bytes(num_seqs, num_heads) : 0;
+    return kda::prefill_rr_workspace_bytes(a);
 }
 
 int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,

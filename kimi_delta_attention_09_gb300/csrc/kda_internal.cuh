@@ -63,26 +63,22 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Chunked prefill on CUDA cores in fp32 (any supported dtype / head size).
 cudaError_t launch_prefill_simt(const PrefillArgs &a, cudaStream_t stream);
 
-// Chunked prefill on tensor cores (bf16 q/k/v with K = V = 128): builder CTAs build each
-// chunk's operand record, scanner CTAs run the serial state chain; records pass through
-// a ring of kWyRing records per scanner in a device workspace.
-constexpr int kWyRing = 8;                       // records per scanner
-constexpr int kWyScanMax = 40;                   // scanner CTAs at most
-constexpr size_t kWyRecordBytes = 74752;         // one chunk's operand record
-constexpr int kStatusTimeout = 1;                // device status word: a bounded wait ran out
-// Workspace bytes for S scanners: status / abort words, per-scanner counters and ring
-// flags, then the records (1024-byte aligned).
-constexpr size_t wy_workspace_bytes_for(int S)
-{
-    return (((size_t)128 + (size_t)S * 64 + (size_t)S * kWyRing * 8 + 1023) / 1024) * 1024 +
-           (size_t)S * kWyRing * kWyRecordBytes;
-}
-bool prefill_wy_supported(const PrefillArgs &a);
-size_t prefill_wy_workspace_bytes(int64_t num_seqs, int32_t num_heads);
-// workspace: zero-filled before its first use; reusable afterwards without clearing
-cudaError_t launch_prefill_wy(const PrefillArgs &a, void *workspace, cudaStream_t stream);
+// Chunked prefill on tensor cores (bf16 q/k/v with K = V = 128): one 4-CTA cluster per
+// (sequence, head) work item; the per-chunk operands are built once per head and shared
+// through a ring of records in a device workspace.
+bool prefill_rr_supported(const PrefillArgs &a);
+constexpr size_t kPrefillRrRecordBytes = 66816;   // one chunk's operand record
+constexpr int kPrefillRrRing = 8;                 // records per cluster
+constexpr size_t kPrefillRrHeaderBytes = 256;     // workspace header: device status word
+constexpr int kStatusTimeout = 1;                 // status word: a bounded wait ran out
+// bytes for min(N H, resident clusters) clusters on the current device
+size_t prefill_rr_workspace_bytes(const PrefillArgs &a);
+// the launch uses min(N H, resident clusters, clusters the workspace holds) clusters
+cudaError_t launch_prefill_rr(const PrefillArgs &a, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream);
 // limit of every wait inside the prefill kernel (0: the default of 2 s)
 void set_prefill_wait_limit_ns(unsigned long long ns);
+
 // One-token paged decode.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 

@@ -1,6 +1,6 @@
-"""kda_chunk_prefill_ws (the tensor-core prefill: builder CTAs hand each chunk's operand
-record to the scanner CTA of its (sequence, head) through a ring in the caller's
-workspace) on the GPU against the fp64 oracle, through the C ABI."""
+"""kda_chunk_prefill_ws (the tensor-core prefill: the four CTAs of a cluster share each
+chunk's operand record through a ring in the caller's workspace) on the GPU against the
+fp64 oracle, through the C ABI."""
 import numpy as np
 import pytest
 import torch
@@ -52,7 +52,7 @@ def test_workspace_size_query():
     from kimi_delta_attention_09_gb300 import _native
     n = _native.kda_chunk_prefill_workspace_bytes(1, 32, 128, 128, torch.bfloat16)
     assert n > 0 and n % 16 == 0
-    # bounded by the largest scanner count, not by the number of sequences
+    # bounded by the resident clusters, not by the number of sequences
     assert _native.kda_chunk_prefill_workspace_bytes(4096, 32, 128, 128, torch.bfloat16) <= 64 * n
     assert _native.kda_chunk_prefill_workspace_bytes(1, 32, 128, 128, torch.float32) == 0
     assert _native.kda_chunk_prefill_workspace_bytes(1, 32, 64, 128, torch.bfloat16) == 0
@@ -66,9 +66,9 @@ def test_ragged_varlen_with_initial_state():
     check_case(case)
 
 
-def test_more_work_items_than_scanners():
-    """80 (sequence, head) items, empty ones included: each scanner walks several items
-    and the record ring wraps many times."""
+def test_more_work_items_than_clusters():
+    """80 (sequence, head) items, empty ones included: each persistent cluster walks
+    several items and the record ring wraps many times."""
     case = inputs.prefill_case([0, 5, 64, 130, 1, 200, 0, 77, 300, 65], H=8, K=128, V=128,
                                dtype="bf16", seed=161, init_std=0.02)
     out, fin = check_case(case)
@@ -78,7 +78,7 @@ def test_more_work_items_than_scanners():
 
 def test_many_short_ragged_sequences():
     """40 and 70 sequences of ragged lengths (ties and empty ones included): each
-    scanner walks several items of different lengths."""
+    persistent cluster walks several items of different lengths."""
     rng = np.random.default_rng(165)
     for n_seqs in (40, 70):
         lens = [int(x) for x in rng.integers(0, 160, size=n_seqs)]
@@ -138,7 +138,7 @@ def test_two_calls_with_one_workspace():
 
 
 def test_strong_gates():
-    """Gates down to -5 per step per channel: the exact-exponential path in the builder."""
+    """Gates down to -5 per step per channel: the exact-exponential path of the builders."""
     case = inputs.prefill_case([150], H=2, K=128, V=128, dtype="bf16", seed=166)
     gen = torch.Generator().manual_seed(166)
     case.g = (-5.0 * torch.rand(case.g.shape, generator=gen)).float()
@@ -185,8 +185,8 @@ def test_large_state_and_value_magnitudes():
 
 
 def test_timeout_is_reported_and_the_context_stays_usable():
-    """A wait limit of 100 ns makes the kernel's waits run out on purpose: the launch
-    ends early, kda_chunk_prefill_status reports KDA_ERR_TIMEOUT (once), and a normal
+    """A wait limit of 100 ns makes the kernel's waits run out on purpose: the clusters
+    end early, kda_chunk_prefill_status reports KDA_ERR_TIMEOUT (once), and a normal
     launch afterwards on the same workspace is correct."""
     from kimi_delta_attention_09_gb300 import _native
     case = inputs.prefill_case([640, 100], H=4, K=128, V=128, dtype="bf16", seed=178,
@@ -304,7 +304,7 @@ def test_paged_ws_reads_and_writes_its_slots():
 
 def test_paged_ws_out_of_range_slot_and_many_items():
     """An index outside [0, S) reads and writes no slot (zero start, final state dropped);
-    40 sequences x 3 heads are more work items than scanners."""
+    40 sequences x 3 heads are more work items than clusters."""
     lens = [(37 * i) % 150 for i in range(40)]
     case = inputs.prefill_case(lens, H=3, K=128, V=128, dtype="bf16", seed=172)
     gen = torch.Generator().manual_seed(173)

@@ -1,68 +1,43 @@
-"""bench.py's multi-process plumbing on the CPU: two gloo ranks (world size 2).
+"""bench.py under torchrun-style launches, on the CPU.
 
-Each rank runs its own replica of the workload (weak scaling, no data-path
-collective); the only communication is the barrier and the max-over-ranks reduction
-of the step time, which is what these tests exercise.  The reference arm prints one
-line from rank 0 and lets the other ranks exit without work.
+Every call of the library runs on one GPU, so the benchmark of our arm is single-GPU:
+a launch with WORLD_SIZE > 1 (or --gpus > 1) prints one error line from rank 0 and
+exits with status 2 before touching a device.  The reference arm (the fp64 oracle on
+the host cores) prints one line from rank 0 and lets the other ranks exit without work.
 """
 import json
 import os
 import subprocess
 import sys
 
-import pytest
-
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _worker(rank, world, port, q):
-    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
-                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
-    sys.path.insert(0, ROOT)
-    import torch.distributed as dist
-    import bench
-    r, w, _ = bench.dist_setup()
-    assert (r, w) == (rank, world) and dist.get_backend() == "gloo"
-    bench.barrier(w)
-    got = bench.max_over_ranks(1.5 + rank, w)   # per-rank step times 1.5 and 2.5 ms
-    q.put((rank, got))
-    dist.barrier()
-    dist.destroy_process_group()
+def _run(rank, world, *extra):
+    env = dict(os.environ, RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+               MASTER_ADDR="127.0.0.1", MASTER_PORT="29555")
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *extra], env=env,
+                          capture_output=True, text=True, timeout=600, cwd=ROOT)
 
 
-def _free_port():
-    import socket
-    s = socket.socket()
-    s.bind(("127.0.0.1", 0))
-    port = s.getsockname()[1]
-    s.close()
-    return port
-
-
-def test_max_over_ranks_gloo_world2():
-    import torch.multiprocessing as mp
-    ctx = mp.get_context("spawn")
-    q = ctx.Queue()
-    port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(timeout=120)
-        assert p.exitcode == 0
-    results = dict(q.get(timeout=5) for _ in range(2))
-    assert results == {0: 2.5, 1: 2.5}
+def test_our_arm_refuses_more_than_one_gpu():
+    for rank in (0, 1):
+        r = _run(rank, 2, "--steps", "1", "--warmup", "3")
+        assert r.returncode == 2, r.stderr[-2000:]
+        if rank == 0:
+            line = json.loads(r.stdout.strip())
+            assert "single-GPU" in line["error"] and line["n_gpus"] == 2
+        else:
+            assert r.stdout.strip() == ""
+    r = _run(0, 1, "--gpus", "4", "--steps", "1")
+    assert r.returncode == 2 and json.loads(r.stdout.strip())["n_gpus"] == 4
 
 
 def test_reference_arm_world2_prints_once():
     """Under torchrun-style env vars the oracle arm runs on rank 0 only."""
     outs = []
     for rank in (0, 1):
-        env = dict(os.environ, RANK=str(rank), WORLD_SIZE="2", LOCAL_RANK=str(rank),
-                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(_free_port()))
-        r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                            "--steps", "1", "--warmup", "3"], env=env, capture_output=True,
-                           text=True, timeout=600, cwd=ROOT)
+        r = _run(rank, 2, "--impl", "reference", "--steps", "1", "--warmup", "3")
         assert r.returncode == 0, r.stderr[-2000:]
         outs.append(r.stdout.strip())
     assert outs[1] == ""
