@@ -94,6 +94,18 @@ enum kda_dtype {
     KDA_DTYPE_BF16 = 1
 };
 
+/*
+ * Option bits of the `flags` argument of the prefill and decode calls.
+ *
+ * KDA_FLAG_QK_L2NORM: normalise every query and key row over the key dimension inside
+ *   the kernel, q <- q / sqrt(sum_c q_c^2 + 1e-6) and likewise k, before it is used --
+ *   the in-kernel half of the fused prologue of the prompt path (vllm.cpp PR #110,
+ *   commit description: chunk_kda_with_fused_gate), which reads unit-scale keys.  The
+ *   rows are normalised where the kernels load them, so the option reads no extra
+ *   bytes.  Without it q and k are used as given (callers normalise them).
+ */
+#define KDA_FLAG_QK_L2NORM 1
+
 enum kda_status {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = -1,   /* null required pointer, negative size, misaligned pointer,
@@ -145,6 +157,7 @@ KDA_API int kda_last_cuda_error(void);
  *                                                 empty one), or NULL to skip.  May be
  *                                                 exactly init_state.
  *   total_tokens, num_seqs >= 0; H >= 1; K, V in {64, 128}; dtype, out_dtype kda_dtypes.
+ *   flags        KDA_FLAG_* bits (KDA_FLAG_QK_L2NORM); any other bit: KDA_ERR_INVALID_ARG.
  *
  * bf16 q/k/v with K = V = 128 run on the tensor-core cluster kernel with the library's
  * scratch (one such call in flight per device, see "Prefill scratch"; any batch size: the
@@ -157,7 +170,7 @@ KDA_API int kda_chunk_prefill(const void *q, const void *k, const void *v,
                               void *out, float *final_state,
                               int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
                               int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                              int32_t out_dtype, void *stream);
+                              int32_t out_dtype, int32_t flags, void *stream);
 
 /*
  * Bytes of workspace kda_chunk_prefill_ws needs for these sizes on the CURRENT device:
@@ -196,7 +209,7 @@ KDA_API int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
                                  int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
                                  int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
                                  int32_t out_dtype, void *workspace, size_t workspace_bytes,
-                                 void *stream);
+                                 int32_t flags, void *stream);
 
 /*
  * kda_chunk_prefill for callers that cannot allocate device memory.  The pages have no
@@ -207,7 +220,8 @@ KDA_API int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
  * for 48 clusters; zero at load, present from load until exit); the address is looked up
  * on each call with cudaGetSymbolAddress, and no call allocates or frees anything.
  *
- * Arguments, results and errors as for kda_chunk_prefill (which uses the same array).
+ * Arguments, results and errors as for kda_chunk_prefill (which uses the same array),
+ * without the flags argument: q and k are used as given.
  * Every call on a device uses the SAME array, which keeps the last call's contents:
  * two calls whose executions overlap (on different streams, or from different host
  * threads without ordering) race on it and give wrong results; calls enqueued on one
@@ -270,7 +284,7 @@ KDA_API int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
                                     const int32_t *cu_seqlens, void *out,
                                     int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
                                     int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
-                                    int32_t dtype, int32_t out_dtype, void *stream);
+                                    int32_t dtype, int32_t out_dtype, int32_t flags, void *stream);
 
 /*
  * kda_chunk_prefill_paged with a caller workspace: the same operation with the
@@ -285,7 +299,7 @@ KDA_API int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void 
                                        int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
                                        int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
                                        int32_t dtype, int32_t out_dtype, void *workspace,
-                                       size_t workspace_bytes, void *stream);
+                                       size_t workspace_bytes, int32_t flags, void *stream);
 
 /*
  * One recurrent decode step for num_seqs sequences with paged states.
@@ -307,13 +321,15 @@ KDA_API int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void 
  *                                           An index outside [0, num_slots) touches
  *                                           no slot and gives zero outputs.
  *   out          [num_seqs, H, V]  out_dtype
+ *   flags        KDA_FLAG_* bits as for kda_chunk_prefill (KDA_FLAG_QK_L2NORM normalises
+ *                the token's q and k rows before the step)
  */
 KDA_API int kda_recurrent_decode(const void *q, const void *k, const void *v,
                                  const float *g, const float *beta, float scale,
                                  float *state_pool, const int32_t *state_idx, void *out,
                                  int32_t num_seqs, int32_t num_slots, int32_t num_heads,
                                  int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                                 int32_t out_dtype, void *stream);
+                                 int32_t out_dtype, int32_t flags, void *stream);
 
 /*
  * kda_recurrent_decode over a pool stored in bf16: the same step, the same
@@ -336,7 +352,7 @@ KDA_API int kda_recurrent_decode_bf16_state(const void *q, const void *k, const 
                                             void *state_pool, const int32_t *state_idx, void *out,
                                             int32_t num_seqs, int32_t num_slots, int32_t num_heads,
                                             int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                                            int32_t out_dtype, void *stream);
+                                            int32_t out_dtype, int32_t flags, void *stream);
 
 #ifdef __cplusplus
 }

@@ -53,13 +53,14 @@ def prefill_workspace(num_seqs, num_heads, head_dim_k, head_dim_v, dtype, device
 
 def chunk_prefill(q, k, v, g, beta, scale=None, init_state=None, cu_seqlens=None,
                   output_final_state: bool = True, final_state=None, out_dtype=None,
-                  stream=None, workspace=None):
+                  stream=None, workspace=None, qk_l2norm: bool = False):
     """Chunked KDA prefill of packed sequences (CUDA tensors, layouts of include/kda.h).
 
     Returns ``(out, final_state)``; ``final_state`` is None when not requested.
     Passing ``final_state=init_state`` carries the state in place.  ``out_dtype``
-    defaults to the dtype of ``v``.  Runs ``kda_chunk_prefill_ws`` with ``workspace``,
-    or with the cached workspace of ``prefill_workspace`` when None.
+    defaults to the dtype of ``v``.  ``qk_l2norm`` normalises the q and k rows inside
+    the kernel.  Runs ``kda_chunk_prefill_ws`` with ``workspace``, or with the cached
+    workspace of ``prefill_workspace`` when None.
     """
     import torch
     from . import _native
@@ -76,12 +77,13 @@ def chunk_prefill(q, k, v, g, beta, scale=None, init_state=None, cu_seqlens=None
     if workspace is None:
         workspace = prefill_workspace(N, H, K, V, q.dtype, q.device, stream)
     _native.kda_chunk_prefill_ws(q, k, v, g, beta, scale, init_state, cu_seqlens, out,
-                                 final_state, workspace, stream)
+                                 final_state, workspace, stream,
+                                 _native.KDA_FLAG_QK_L2NORM if qk_l2norm else 0)
     return out, final_state
 
 
 def chunk_prefill_paged(q, k, v, g, beta, state_pool, state_idx, scale=None, cu_seqlens=None,
-                        out_dtype=None, stream=None, workspace=None):
+                        out_dtype=None, stream=None, workspace=None, qk_l2norm: bool = False):
     """Chunked prefill with each sequence's state in slot ``state_idx[n]`` of
     ``state_pool`` (read as the initial state, overwritten with the final state).  Runs
     ``kda_chunk_prefill_paged_ws`` with ``workspace`` or the cached one of
@@ -98,12 +100,13 @@ def chunk_prefill_paged(q, k, v, g, beta, state_pool, state_idx, scale=None, cu_
         workspace = prefill_workspace(cu_seqlens.numel() - 1, H, K, v.shape[-1], q.dtype,
                                       q.device, stream)
     _native.kda_chunk_prefill_paged_ws(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens,
-                                       out, workspace, stream)
+                                       out, workspace, stream,
+                                       _native.KDA_FLAG_QK_L2NORM if qk_l2norm else 0)
     return out
 
 
 def recurrent_decode(q, k, v, g, beta, state_pool, state_idx, scale=None, out_dtype=None,
-                     stream=None):
+                     stream=None, qk_l2norm: bool = False):
     """One KDA decode step; ``state_pool`` is updated in place at ``state_idx``.
 
     An fp32 pool runs ``kda_recurrent_decode``; a bf16 pool runs
@@ -113,10 +116,12 @@ def recurrent_decode(q, k, v, g, beta, state_pool, state_idx, scale=None, out_dt
     if scale is None:
         scale = q.shape[-1] ** -0.5
     out = torch.empty(v.shape, dtype=out_dtype or v.dtype, device=v.device)
+    flags = _native.KDA_FLAG_QK_L2NORM if qk_l2norm else 0
     if state_pool.dtype == torch.bfloat16:
-        _native.kda_recurrent_decode_bf16_state(q, k, v, g, beta, scale, state_pool, state_idx, out, stream)
+        _native.kda_recurrent_decode_bf16_state(q, k, v, g, beta, scale, state_pool, state_idx, out,
+                                                stream, flags)
     else:
-        _native.kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out, stream)
+        _native.kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out, stream, flags)
     return out
 
 

@@ -20,6 +20,7 @@ KDA_ERR_CUDA = -4
 KDA_ERR_TIMEOUT = -5
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
+KDA_FLAG_QK_L2NORM = 1
 ABI_VERSION = 4
 
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
@@ -49,32 +50,32 @@ def _load() -> ctypes.CDLL:
     lib.kda_last_cuda_error.argtypes = []
     lib.kda_last_cuda_error.restype = ctypes.c_int
     lib.kda_chunk_prefill.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
-                                      i64, i32, i32, i32, i32, i32, i32, vp]
+                                      i64, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_chunk_prefill.restype = ctypes.c_int
     lib.kda_chunk_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.kda_chunk_prefill_workspace_bytes.restype = ctypes.c_size_t
     lib.kda_chunk_prefill_ws.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
-                                         i64, i32, i32, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]
+                                         i64, i32, i32, i32, i32, i32, i32, vp, ctypes.c_size_t, i32, vp]
     lib.kda_chunk_prefill_ws.restype = ctypes.c_int
     lib.kda_chunk_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
                                               i64, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_chunk_prefill_noalloc.restype = ctypes.c_int
     lib.kda_chunk_prefill_paged.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
-                                            i64, i32, i32, i32, i32, i32, i32, i32, vp]
+                                            i64, i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_chunk_prefill_paged.restype = ctypes.c_int
     lib.kda_chunk_prefill_paged_ws.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
                                                i64, i32, i32, i32, i32, i32, i32, i32, vp,
-                                               ctypes.c_size_t, vp]
+                                               ctypes.c_size_t, i32, vp]
     lib.kda_chunk_prefill_paged_ws.restype = ctypes.c_int
     lib.kda_chunk_prefill_status.argtypes = [vp, vp]
     lib.kda_chunk_prefill_status.restype = ctypes.c_int
     lib.kda_set_prefill_wait_limit.argtypes = [ctypes.c_uint64]
     lib.kda_set_prefill_wait_limit.restype = None
     lib.kda_recurrent_decode.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp,
-                                         i32, i32, i32, i32, i32, i32, i32, vp]
+                                         i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_recurrent_decode.restype = ctypes.c_int
     lib.kda_recurrent_decode_bf16_state.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp,
-                                                    i32, i32, i32, i32, i32, i32, i32, vp]
+                                                    i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_recurrent_decode_bf16_state.restype = ctypes.c_int
     if lib.kda_abi_version() != ABI_VERSION:
         raise RuntimeError(f"libkda.so ABI {lib.kda_abi_version()} != expected {ABI_VERSION}")
@@ -120,7 +121,7 @@ def _need(cond: bool, msg: str):
 
 
 def kda_chunk_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
-                      stream=None) -> None:
+                      stream=None, flags=0) -> None:
     """Enqueue ``kda_chunk_prefill`` on ``stream`` (default: torch's current stream).
 
     Tensors are CUDA tensors laid out as include/kda.h states; shapes and dtypes are
@@ -148,7 +149,7 @@ def kda_chunk_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, out, fina
                   "states must be fp32 [N, H, K, V]")
     rc = lib.kda_chunk_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
                                _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
-                               T, N, H, K, V, _dtype_code(q), _dtype_code(out),
+                               T, N, H, K, V, _dtype_code(q), _dtype_code(out), int(flags),
                                _stream_handle(stream))
     _check("kda_chunk_prefill", rc)
 
@@ -164,7 +165,7 @@ def kda_chunk_prefill_workspace_bytes(num_seqs: int, num_heads: int, head_dim_k:
 
 
 def kda_chunk_prefill_ws(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
-                         workspace, stream=None) -> None:
+                         workspace, stream=None, flags=0) -> None:
     """Enqueue ``kda_chunk_prefill_ws``: as ``kda_chunk_prefill`` plus ``workspace``, a
     contiguous CUDA tensor (any dtype) of at least ``kda_chunk_prefill_workspace_bytes``
     bytes, or None when that is 0."""
@@ -191,7 +192,7 @@ def kda_chunk_prefill_ws(q, k, v, g, beta, scale, init_state, cu_seqlens, out, f
     rc = lib.kda_chunk_prefill_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
                                   _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
                                   T, N, H, K, V, _dtype_code(q), _dtype_code(out), _ptr(workspace),
-                                  ws_bytes, _stream_handle(stream))
+                                  ws_bytes, int(flags), _stream_handle(stream))
     _check("kda_chunk_prefill_ws", rc)
 
 
@@ -226,7 +227,7 @@ def kda_chunk_prefill_noalloc(q, k, v, g, beta, scale, init_state, cu_seqlens, o
 
 
 def kda_chunk_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens, out,
-                            stream=None) -> None:
+                            stream=None, flags=0) -> None:
     """Enqueue ``kda_chunk_prefill_paged``: as ``kda_chunk_prefill`` with sequence n's
     initial and final state in slot ``state_idx[n]`` of ``state_pool`` [S, H, K, V]."""
     T, H, K = q.shape
@@ -250,12 +251,12 @@ def kda_chunk_prefill_paged(q, k, v, g, beta, scale, state_pool, state_idx, cu_s
     rc = lib.kda_chunk_prefill_paged(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
                                      _ptr(state_pool), _ptr(state_idx), _ptr(cu_seqlens),
                                      _ptr(out), T, N, S, H, K, V, _dtype_code(q), _dtype_code(out),
-                                     _stream_handle(stream))
+                                     int(flags), _stream_handle(stream))
     _check("kda_chunk_prefill_paged", rc)
 
 
 def kda_chunk_prefill_paged_ws(q, k, v, g, beta, scale, state_pool, state_idx, cu_seqlens, out,
-                               workspace, stream=None) -> None:
+                               workspace, stream=None, flags=0) -> None:
     """Enqueue ``kda_chunk_prefill_paged_ws``: ``kda_chunk_prefill_paged`` plus ``workspace``
     (as for ``kda_chunk_prefill_ws``)."""
     T, H, K = q.shape
@@ -281,7 +282,7 @@ def kda_chunk_prefill_paged_ws(q, k, v, g, beta, scale, state_pool, state_idx, c
     rc = lib.kda_chunk_prefill_paged_ws(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
                                         _ptr(state_pool), _ptr(state_idx), _ptr(cu_seqlens),
                                         _ptr(out), T, N, S, H, K, V, _dtype_code(q), _dtype_code(out),
-                                        _ptr(workspace), ws_bytes, _stream_handle(stream))
+                                        _ptr(workspace), ws_bytes, int(flags), _stream_handle(stream))
     _check("kda_chunk_prefill_paged_ws", rc)
 
 
@@ -300,7 +301,7 @@ def kda_set_prefill_wait_limit(nanoseconds: int) -> None:
     lib.kda_set_prefill_wait_limit(int(nanoseconds))
 
 
-def _decode(fn, q, k, v, g, beta, scale, state_pool, state_idx, out, pool_dtype, stream):
+def _decode(fn, q, k, v, g, beta, scale, state_pool, state_idx, out, pool_dtype, stream, flags):
     N, H, K = q.shape
     V = v.shape[-1]
     S = state_pool.shape[0]
@@ -318,22 +319,22 @@ def _decode(fn, q, k, v, g, beta, scale, state_pool, state_idx, out, pool_dtype,
     _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g, beta must be fp32")
     rc = getattr(lib, fn)(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
                           _ptr(state_pool), _ptr(state_idx), _ptr(out),
-                          N, S, H, K, V, _dtype_code(q), _dtype_code(out),
+                          N, S, H, K, V, _dtype_code(q), _dtype_code(out), int(flags),
                           _stream_handle(stream))
     _check(fn, rc)
 
 
 def kda_recurrent_decode(q, k, v, g, beta, scale, state_pool, state_idx, out,
-                         stream=None) -> None:
+                         stream=None, flags=0) -> None:
     """Enqueue ``kda_recurrent_decode``: q [N, H, K], v [N, H, V], fp32 pool [S, H, K, V]."""
     import torch
     _decode("kda_recurrent_decode", q, k, v, g, beta, scale, state_pool, state_idx, out,
-            torch.float32, stream)
+            torch.float32, stream, flags)
 
 
 def kda_recurrent_decode_bf16_state(q, k, v, g, beta, scale, state_pool, state_idx, out,
-                                    stream=None) -> None:
+                                    stream=None, flags=0) -> None:
     """Enqueue ``kda_recurrent_decode_bf16_state``: the same step on a bf16 pool [S, H, K, V]."""
     import torch
     _decode("kda_recurrent_decode_bf16_state", q, k, v, g, beta, scale, state_pool, state_idx, out,
-            torch.bfloat16, stream)
+            torch.bfloat16, stream, flags)

@@ -225,7 +225,7 @@ int kda_chunk_prefill(const void *q, const void *k, const void *v,
                       void *out, float *final_state,
                       int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
                       int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                      int32_t out_dtype, void *stream)
+                      int32_t out_dtype, int32_t flags, void *stream)
 {
     kda::PrefillArgs a;
     Range ranges[9];
@@ -233,6 +233,8 @@ int kda_chunk_prefill(const void *q, const void *k, const void *v,
                                  total_tokens, num_seqs, num_heads, head_dim_k, head_dim_v, dtype,
                                  out_dtype, a, ranges);
     if (st != KDA_OK || num_seqs == 0) return st;
+    if (flags & ~kda::kFlagQkL2Norm) return KDA_ERR_INVALID_ARG;
+    a.flags = flags;
     return launch_prefill_static(a, stream);
 }
 
@@ -252,7 +254,7 @@ int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
                          void *out, float *final_state,
                          int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
                          int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                         int32_t out_dtype, void *workspace, size_t workspace_bytes, void *stream)
+                         int32_t out_dtype, void *workspace, size_t workspace_bytes, int32_t flags, void *stream)
 {
     kda::PrefillArgs a;
     Range ranges[9];
@@ -260,6 +262,8 @@ int kda_chunk_prefill_ws(const void *q, const void *k, const void *v,
                                  total_tokens, num_seqs, num_heads, head_dim_k, head_dim_v, dtype,
                                  out_dtype, a, ranges);
     if (st != KDA_OK || num_seqs == 0) return st;
+    if (flags & ~kda::kFlagQkL2Norm) return KDA_ERR_INVALID_ARG;
+    a.flags = flags;
     return launch_prefill_ws(a, ranges, workspace, workspace_bytes, stream);
 }
 
@@ -286,7 +290,7 @@ int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
                             const int32_t *cu_seqlens, void *out,
                             int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
                             int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
-                            int32_t dtype, int32_t out_dtype, void *stream)
+                            int32_t dtype, int32_t out_dtype, int32_t flags, void *stream)
 {
     kda::PrefillArgs a;
     Range ranges[9];
@@ -294,6 +298,8 @@ int kda_chunk_prefill_paged(const void *q, const void *k, const void *v,
                                        out, total_tokens, num_seqs, num_slots, num_heads,
                                        head_dim_k, head_dim_v, dtype, out_dtype, a, ranges);
     if (st != KDA_OK || num_seqs == 0) return st;
+    if (flags & ~kda::kFlagQkL2Norm) return KDA_ERR_INVALID_ARG;
+    a.flags = flags;
     return launch_prefill_static(a, stream);
 }
 
@@ -304,7 +310,7 @@ int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void *v,
                                int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
                                int32_t num_heads, int32_t head_dim_k, int32_t head_dim_v,
                                int32_t dtype, int32_t out_dtype, void *workspace,
-                               size_t workspace_bytes, void *stream)
+                               size_t workspace_bytes, int32_t flags, void *stream)
 {
     kda::PrefillArgs a;
     Range ranges[9];
@@ -312,6 +318,8 @@ int kda_chunk_prefill_paged_ws(const void *q, const void *k, const void *v,
                                        out, total_tokens, num_seqs, num_slots, num_heads,
                                        head_dim_k, head_dim_v, dtype, out_dtype, a, ranges);
     if (st != KDA_OK || num_seqs == 0) return st;
+    if (flags & ~kda::kFlagQkL2Norm) return KDA_ERR_INVALID_ARG;
+    a.flags = flags;
     return launch_prefill_ws(a, ranges, workspace, workspace_bytes, stream);
 }
 
@@ -342,9 +350,10 @@ static int recurrent_decode(const void *q, const void *k, const void *v,
                             void *state_pool, int32_t state_dtype, const int32_t *state_idx, void *out,
                             int32_t num_seqs, int32_t num_slots, int32_t num_heads,
                             int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                            int32_t out_dtype, void *stream)
+                            int32_t out_dtype, int32_t flags, void *stream)
 {
-    if (num_seqs < 0 || num_slots < 0 || num_heads < 1 || !std::isfinite(scale))
+    if (num_seqs < 0 || num_slots < 0 || num_heads < 1 || !std::isfinite(scale) ||
+        (flags & ~kda::kFlagQkL2Norm))
         return KDA_ERR_INVALID_ARG;
     if (!dtype_supported(dtype) || !dtype_supported(out_dtype)) return KDA_ERR_UNSUPPORTED;
     if (!dims_supported(head_dim_k) || !dims_supported(head_dim_v)) return KDA_ERR_UNSUPPORTED;
@@ -372,7 +381,7 @@ static int recurrent_decode(const void *q, const void *k, const void *v,
     a.pool = state_pool; a.state_idx = state_idx; a.out = out;
     a.num_seqs = num_seqs; a.num_slots = num_slots; a.num_heads = num_heads;
     a.head_dim_k = head_dim_k; a.head_dim_v = head_dim_v; a.dtype = dtype;
-    a.out_dtype = out_dtype; a.state_dtype = state_dtype;
+    a.out_dtype = out_dtype; a.state_dtype = state_dtype; a.flags = flags;
     return finish(kda::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -381,11 +390,11 @@ int kda_recurrent_decode(const void *q, const void *k, const void *v,
                          float *state_pool, const int32_t *state_idx, void *out,
                          int32_t num_seqs, int32_t num_slots, int32_t num_heads,
                          int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                         int32_t out_dtype, void *stream)
+                         int32_t out_dtype, int32_t flags, void *stream)
 {
     return recurrent_decode(q, k, v, g, beta, scale, state_pool, KDA_DTYPE_F32, state_idx, out,
                             num_seqs, num_slots, num_heads, head_dim_k, head_dim_v, dtype,
-                            out_dtype, stream);
+                            out_dtype, flags, stream);
 }
 
 int kda_recurrent_decode_bf16_state(const void *q, const void *k, const void *v,
@@ -393,11 +402,11 @@ int kda_recurrent_decode_bf16_state(const void *q, const void *k, const void *v,
                                     void *state_pool, const int32_t *state_idx, void *out,
                                     int32_t num_seqs, int32_t num_slots, int32_t num_heads,
                                     int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
-                                    int32_t out_dtype, void *stream)
+                                    int32_t out_dtype, int32_t flags, void *stream)
 {
     return recurrent_decode(q, k, v, g, beta, scale, state_pool, KDA_DTYPE_BF16, state_idx, out,
                             num_seqs, num_slots, num_heads, head_dim_k, head_dim_v, dtype,
-                            out_dtype, stream);
+                            out_dtype, flags, stream);
 }
 
 }  // extern "C"

@@ -7,7 +7,9 @@
 // per-sequence state indices).  The gather, the update and the scatter are fused:
 // every selected state is read from HBM once and written back once.
 //
-// Per (sequence n, head h), with S = pool[state_idx[n], h] (K x V, row = key channel):
+// Per (sequence n, head h), with S = pool[state_idx[n], h] (K x V, row = key channel) and,
+// with the in-kernel L2 normalisation, k and q first scaled to unit norm over K (the
+// norms reduce beside S^T k and S^T q, and every product is linear in k and in q):
 //     S <- Diag(exp g) S;   u = S^T k;   d = beta (v - u);   S <- S + k d^T;
 //     o  = scale S^T q = scale ((Diag(exp g) S_old)^T q + (k.q) d)
 // so S is read once, both reductions (against k and q) run on the decayed state,
@@ -81,8 +83,9 @@ kda_decode_kernel(DecodeArgs a)
         dr[j] = expf(gp[c]);
     }
 
-    // decay, then partial reductions against k and q (and k.q) over this thread's rows
-    float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f}, kq = 0.f;
+    // decay, then partial reductions against k and q (and k.q, |k|^2, |q|^2) over this
+    // thread's rows
+    float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f}, kq = 0.f, kk = 0.f, qq = 0.f;
 #pragma unroll
     for (int j = 0; j < kRowsPerThread; ++j) {
         s[j].x *= dr[j]; s[j].y *= dr[j]; s[j].z *= dr[j]; s[j].w *= dr[j];
@@ -91,6 +94,8 @@ kda_decode_kernel(DecodeArgs a)
         pq[0] += s[j].x * qr[j]; pq[1] += s[j].y * qr[j];
         pq[2] += s[j].z * qr[j]; pq[3] += s[j].w * qr[j];
         kq += kr[j] * qr[j];
+        kk += kr[j] * kr[j];
+        qq += qr[j] * qr[j];
     }
     // reduce over the 4 row groups of this warp (lanes differing in bits 3, 4)
 #pragma unroll
@@ -101,24 +106,38 @@ kda_decode_kernel(DecodeArgs a)
             pq[i] += __shfl_xor_sync(0xffffffffu, pq[i], off);
         }
         kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        kk += __shfl_xor_sync(0xffffffffu, kk, off);
+        qq += __shfl_xor_sync(0xffffffffu, qq, off);
     }
     // ... and over the 4 warps
-    __shared__ float red[kDecThreads / 32][8][9];
+    __shared__ float red[kDecThreads / 32][8][11];
     const int warp = tid >> 5, lane = tid & 31;
     if (lane < 8) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) { red[warp][lane][i] = pk[i]; red[warp][lane][4 + i] = pq[i]; }
         red[warp][lane][8] = kq;
+        red[warp][lane][9] = kk;
+        red[warp][lane][10] = qq;
     }
     __syncthreads();
     float u[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
-    kq = 0.f;
+    kq = kk = qq = 0.f;
 #pragma unroll
     for (int w = 0; w < kDecThreads / 32; ++w) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) { u[i] += red[w][cg][i]; qs[i] += red[w][cg][4 + i]; }
         kq += red[w][cg][8];
+        kk += red[w][cg][9];
+        qq += red[w][cg][10];
     }
+    // in-kernel L2 normalisation: every product above is linear in k and in q
+    const float rk = (a.flags & kFlagQkL2Norm) ? rsqrtf(kk + kQkL2NormEps) : 1.f;
+    const float rq = (a.flags & kFlagQkL2Norm) ? rsqrtf(qq + kQkL2NormEps) : 1.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { u[i] *= rk; qs[i] *= rq; }
+    kq *= rk * rq;
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; ++j) kr[j] *= rk;
 
     const float beta = a.beta[n * H + h];
     const Tin *vp = static_cast<const Tin *>(a.v) + (n * H + h) * V + col0;
@@ -198,7 +217,7 @@ kda_decode_bf16_state_kernel(DecodeArgs a)
             x[2 * e + 1] = f.y * dr[j];
         }
     };
-    float pk[8], pq[8], kq = 0.f;
+    float pk[8], pq[8], kq = 0.f, kk = 0.f, qq = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) pk[i] = pq[i] = 0.f;
 #pragma unroll
@@ -208,6 +227,8 @@ kda_decode_bf16_state_kernel(DecodeArgs a)
 #pragma unroll
         for (int i = 0; i < 8; ++i) { pk[i] += x[i] * kr[j]; pq[i] += x[i] * qr[j]; }
         kq += kr[j] * qr[j];
+        kk += kr[j] * kr[j];
+        qq += qr[j] * qr[j];
     }
 #pragma unroll
     for (int off = 8; off <= 16; off <<= 1) {
@@ -217,25 +238,39 @@ kda_decode_bf16_state_kernel(DecodeArgs a)
             pq[i] += __shfl_xor_sync(0xffffffffu, pq[i], off);
         }
         kq += __shfl_xor_sync(0xffffffffu, kq, off);
+        kk += __shfl_xor_sync(0xffffffffu, kk, off);
+        qq += __shfl_xor_sync(0xffffffffu, qq, off);
     }
-    __shared__ float red[kDecThreads / 32][8][17];
+    __shared__ float red[kDecThreads / 32][8][19];
     const int warp = tid >> 5, lane = tid & 31;
     if (lane < 8) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) { red[warp][lane][i] = pk[i]; red[warp][lane][8 + i] = pq[i]; }
         red[warp][lane][16] = kq;
+        red[warp][lane][17] = kk;
+        red[warp][lane][18] = qq;
     }
     __syncthreads();
     float u[8], qs[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) u[i] = qs[i] = 0.f;
-    kq = 0.f;
+    kq = kk = qq = 0.f;
 #pragma unroll
     for (int w = 0; w < kDecThreads / 32; ++w) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) { u[i] += red[w][cg][i]; qs[i] += red[w][cg][8 + i]; }
         kq += red[w][cg][16];
+        kk += red[w][cg][17];
+        qq += red[w][cg][18];
     }
+    // in-kernel L2 normalisation: every product above is linear in k and in q
+    const float rk = (a.flags & kFlagQkL2Norm) ? rsqrtf(kk + kQkL2NormEps) : 1.f;
+    const float rq = (a.flags & kFlagQkL2Norm) ? rsqrtf(qq + kQkL2NormEps) : 1.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { u[i] *= rk; qs[i] *= rq; }
+    kq *= rk * rq;
+#pragma unroll
+    for (int j = 0; j < kRowsPerThread; ++j) kr[j] *= rk;
 
     const float beta = a.beta[n * H + h];
     const Tin *vp = static_cast<const Tin *>(a.v) + (n * H + h) * V + col0;

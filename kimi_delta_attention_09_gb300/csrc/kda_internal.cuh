@@ -22,6 +22,7 @@ struct PrefillArgs {
     int32_t num_slots;
     int64_t total_tokens;
     int32_t num_seqs, num_heads, head_dim_k, head_dim_v, dtype, out_dtype;
+    int32_t flags;                // kFlag* bits
 };
 
 // Base pointers of the (sequence n, head h) state for a prefill: the caller's
@@ -53,8 +54,11 @@ struct DecodeArgs {
     const int32_t *state_idx;     // [N]
     void *out;                    // [N, H, V], out_dtype
     int32_t num_seqs, num_slots, num_heads, head_dim_k, head_dim_v, dtype, out_dtype, state_dtype;
+    int32_t flags;                // kFlag* bits
 };
 
+constexpr int kFlagQkL2Norm = 1;        // normalise q and k rows over K in the kernel
+constexpr float kQkL2NormEps = 1e-6f;   // q / sqrt(sum q^2 + eps)
 constexpr int kDtypeF32 = 0;
 constexpr int kDtypeBF16 = 1;
 constexpr int kChunk = 64;              // tokens per prefill chunk

@@ -143,7 +143,9 @@ struct Smem {
     static constexpr int consumed = bars + Bar::count * 8;   // i64: chunks whose record this CTA has
     static constexpr int tmem = consumed + 8;                // u32
     static constexpr int flag = tmem + 4;
-    static constexpr int total = flag + 4;
+    static constexpr int nred = (flag + 4 + 15) / 16 * 16;  // builder: f32 [8 warps][32] row |x|^2 sums
+    static constexpr int nscl = nred + 8 * 32 * 4;           // builder: f32 [4][q 16 | k 16] 1/|x| per row
+    static constexpr int total = nscl + 4 * 32 * 4;
 };
 static_assert(Smem::total <= 232448, "shared memory budget");
 static_assert(Smem::slot_bytes % 1024 == 0 && Smem::ht % 1024 == 0 && Smem::dt % 1024 == 0 &&
@@ -251,9 +253,15 @@ __device__ __forceinline__ bool cursor_next(Cursor &c, const PrefillArgs &a, int
 // Exact-exponential A_kk (to shared memory), A_qk and K^^T (to the record in global
 // memory) for a chunk whose gate span leaves the fp16 fast path: one exponential per
 // pair and channel.  G is the chunk's exp2-space cumsum, fp32 [64][128], in global scratch.
+// With the in-kernel L2 normalisation, nscl holds the rows' 1/|q| and 1/|k| (else null).
+__device__ __forceinline__ float row_scale(const float *nscl, int r, int is_k)
+{
+    return nscl ? nscl[(r >> 4) * 32 + 16 * is_k + (r & 15)] : 1.f;
+}
 __device__ __noinline__ void exact_pairs(const PrefillArgs &a, int64_t t0, int len, int h,
                                          const float *G, const float *bs, __half *akk,
-                                         unsigned char *aqk_g, unsigned char *kht_g, int gtid)
+                                         unsigned char *aqk_g, unsigned char *kht_g, int gtid,
+                                         const float *nscl)
 {
     const int H = a.num_heads;
     const __nv_bfloat16 *kk = static_cast<const __nv_bfloat16 *>(a.k);
@@ -269,6 +277,9 @@ __device__ __noinline__ void exact_pairs(const PrefillArgs &a, int64_t t0, int l
                 sk += __bfloat162float(kr[c]) * kic;
                 sq += __bfloat162float(qr[c]) * kic;
             }
+            const float si = row_scale(nscl, i, 1);
+            sk *= si * row_scale(nscl, r, 1);
+            sq *= si * row_scale(nscl, r, 0);
         }
         akk[sw128(r, i, C)] = __float2half_rn(i < r ? bs[r] * sk : 0.f);
         reinterpret_cast<__half *>(aqk_g)[sw128(r, i, C)] = __float2half_rn(i <= r ? sq : 0.f);
@@ -277,13 +288,13 @@ __device__ __noinline__ void exact_pairs(const PrefillArgs &a, int64_t t0, int l
     // can leave the fp32 range at such spans); rows past the end have G = G_last
     for (int e = gtid; e < C * KD; e += kGroup) {
         const int r = e >> 7, c = e & 127;
-        const float kv = r < len ? __bfloat162float(kk[((t0 + r) * H + h) * KD + c]) : 0.f;
+        const float kv = r < len ? __bfloat162float(kk[((t0 + r) * H + h) * KD + c]) * row_scale(nscl, r, 1) : 0.f;
         reinterpret_cast<__half *>(kht_g)[sw128(c, r, KD)] =
             __float2half_rn(kv * exp2f(G[(C - 1) * KD + c] - G[r * KD + c]));
     }
 }
 
-template <typename Tout>
+template <typename Tout, bool kL2>
 __global__ void __cluster_dims__(kRanks, 1, 1) __launch_bounds__(kThreads, 1)
 kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                       unsigned char *__restrict__ ws, int G, const RrWait wt)
@@ -339,6 +350,9 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
         float *decs = reinterpret_cast<float *>(sm + Smem::st_vec + (Rec::dec - Rec::beta));
         float *pms = reinterpret_cast<float *>(sm + Smem::st_vec + (Rec::pm - Rec::beta));
         volatile int *flag = reinterpret_cast<volatile int *>(sm + Smem::flag);
+        float *nred = reinterpret_cast<float *>(sm + Smem::nred);
+        float *nscl = reinterpret_cast<float *>(sm + Smem::nscl);
+        constexpr bool l2 = kL2;   // in-kernel L2 normalisation of the q and k rows
         const float *gin = a.g;
         const __nv_bfloat16 *qin = static_cast<const __nv_bfloat16 *>(a.q);
         const __nv_bfloat16 *kin = static_cast<const __nv_bfloat16 *>(a.k);
@@ -401,7 +415,37 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
             *reinterpret_cast<float2 *>(tot + pE * KD + pc0) = gx[15];
             if (pE == 0) *reinterpret_cast<float2 *>(first + pc0) = gx[0];
             if (gtid < C) bs[gtid] = gtid < len ? a.beta[(t0 + gtid) * H + h] : 0.f;
+            if (l2) {
+                // |q_r|^2 (values 0..15) and |k_r|^2 (16..31) of this thread's rows over its two
+                // channels, reduced over the warp so that lane L ends with value L summed over
+                // the warp's 64 channels (halving exchanges, 31 shuffles)
+                float nv[32];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq[u]));
+                    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kq[u]));
+                    nv[u] = qv.x * qv.x + qv.y * qv.y;
+                    nv[16 + u] = kv.x * kv.x + kv.y * kv.y;
+                }
+#pragma unroll
+                for (int w = 16; w >= 1; w >>= 1) {
+                    const bool up = (lane & w) != 0;
+#pragma unroll
+                    for (int i = 0; i < w; ++i) {
+                        const float send = up ? nv[i] : nv[i + w];
+                        const float keep = up ? nv[i + w] : nv[i];
+                        nv[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+                    }
+                }
+                nred[(gtid >> 5) * 32 + lane] = nv[0];
+            }
             named_bar_sync(kBarBuild, kGroup);
+            if (l2) {   // the two warps of a 16-row group hold the halves of its 128 channels
+                const int gw = gtid >> 5;
+                if ((gw & 1) == 0)
+                    nscl[(gw >> 1) * 32 + lane] = rsqrtf(nred[gw * 32 + lane] + nred[(gw + 1) * 32 + lane] + kQkL2NormEps);
+                named_bar_sync(kBarBuild, kGroup);
+            }
 
             // ---------------- P2: reference, factors, fp16 operands; K^^T straight to the record
             float2 pre = make_float2(0.f, 0.f), run = make_float2(0.f, 0.f);
@@ -434,8 +478,12 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                     amax = fmaxf(amax, fmaxf(fabsf(xx), fabsf(xy)));
                     const float ex = exp2f(xx), ey = exp2f(xy);
                     const float ix = rcp_approx(ex), iy = rcp_approx(ey);
-                    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kq[8 * hb + u]));
-                    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq[8 * hb + u]));
+                    float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kq[8 * hb + u]));
+                    float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq[8 * hb + u]));
+                    if (l2) {
+                        const float sq = nscl[pE * 32 + 8 * hb + u], sk = nscl[pE * 32 + 16 + 8 * hb + u];
+                        qv.x *= sq; qv.y *= sq; kv.x *= sk; kv.y *= sk;
+                    }
                     *reinterpret_cast<uint32_t *>(aop + sw128(r, pc0, 2 * C)) = pack_h2(kv.x * ex, kv.y * ey);
                     *reinterpret_cast<uint32_t *>(aop + sw128(C + r, pc0, 2 * C)) = pack_h2(qv.x * ex, qv.y * ey);
                     const float b0 = kv.x * ix, b1 = kv.y * iy;
@@ -511,7 +559,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                     *reinterpret_cast<float2 *>(Gs + r * KD + pc0) = make_float2(gx[u].x + pre.x, gx[u].y + pre.y);
                 }
                 named_bar_sync(kBarBuild, kGroup);
-                exact_pairs(a, t0, len, h, Gs, bs, akk, aqk_g, rec + Rec::kht, gtid);
+                exact_pairs(a, t0, len, h, Gs, bs, akk, aqk_g, rec + Rec::kht, gtid, l2 ? nscl : nullptr);
             }
             if (!exact_path) fence_proxy_async_smem();   // A_qk is read by the bulk copy
             named_bar_sync(kBarBuild, kGroup);   // A_kk complete; the G scratch is no longer read
@@ -824,13 +872,13 @@ int max_clusters()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
     if (cached[dev] > 0) return cached[dev];
     int n = 0;
-    if (cudaFuncSetAttribute(kda_prefill_rr_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kda_prefill_rr_kernel<__nv_bfloat16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Smem::total) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(kRanks * 1024);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = Smem::total;
-        if (cudaOccupancyMaxActiveClusters(&n, kda_prefill_rr_kernel<__nv_bfloat16>, &cfg) != cudaSuccess) n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kda_prefill_rr_kernel<__nv_bfloat16, false>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();   // a failed query leaves no sticky error behind
     if (n <= 0) {
@@ -854,7 +902,7 @@ int64_t rr_clusters(int64_t items, size_t ring_records)
 
 std::atomic<unsigned long long> g_wait_ns{2000000000ull};
 
-template <typename Tout>
+template <typename Tout, bool kL2>
 cudaError_t launch_rr_t(const PrefillArgs &a, void *ws, size_t ws_bytes, cudaStream_t stream)
 {
     RrMaps maps;
@@ -869,7 +917,7 @@ cudaError_t launch_rr_t(const PrefillArgs &a, void *ws, size_t ws_bytes, cudaStr
             return cudaErrorInvalidValue;
         maps.beta_map = (H % 4 == 0) && encode_map_2d(&maps.beta, a.beta, T, H);
     }
-    cudaError_t e = cudaFuncSetAttribute(kda_prefill_rr_kernel<Tout>,
+    cudaError_t e = cudaFuncSetAttribute(kda_prefill_rr_kernel<Tout, kL2>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::total);
     if (e != cudaSuccess) return e;
     const size_t records = ws_bytes > (size_t)kWsHeader ? (ws_bytes - kWsHeader) / Rec::bytes : 0;
@@ -877,7 +925,7 @@ cudaError_t launch_rr_t(const PrefillArgs &a, void *ws, size_t ws_bytes, cudaStr
     if (G < 1) return cudaErrorInvalidValue;
     unsigned char *base = static_cast<unsigned char *>(ws);
     const RrWait wt{reinterpret_cast<int *>(base), g_wait_ns.load()};
-    kda_prefill_rr_kernel<Tout><<<(unsigned)(G * kRanks), kThreads, Smem::total, stream>>>(
+    kda_prefill_rr_kernel<Tout, kL2><<<(unsigned)(G * kRanks), kThreads, Smem::total, stream>>>(
         a, maps, base + kWsHeader, (int)G, wt);
     return cudaGetLastError();
 }
@@ -901,8 +949,12 @@ cudaError_t launch_prefill_rr(const PrefillArgs &a, void *workspace, size_t work
                               cudaStream_t stream)
 {
     if (a.num_seqs == 0) return cudaSuccess;
-    return a.out_dtype == kDtypeBF16 ? launch_rr_t<__nv_bfloat16>(a, workspace, workspace_bytes, stream)
-                                     : launch_rr_t<float>(a, workspace, workspace_bytes, stream);
+    const bool l2 = (a.flags & kFlagQkL2Norm) != 0;
+    if (a.out_dtype == kDtypeBF16)
+        return l2 ? launch_rr_t<__nv_bfloat16, true>(a, workspace, workspace_bytes, stream)
+                  : launch_rr_t<__nv_bfloat16, false>(a, workspace, workspace_bytes, stream);
+    return l2 ? launch_rr_t<float, true>(a, workspace, workspace_bytes, stream)
+              : launch_rr_t<float, false>(a, workspace, workspace_bytes, stream);
 }
 
 void set_prefill_wait_limit_ns(unsigned long long ns)

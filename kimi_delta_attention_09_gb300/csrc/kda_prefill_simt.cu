@@ -31,6 +31,7 @@ namespace {
 
 constexpr int kSimtThreads = 256;
 constexpr int kVT = 32;            // V columns per CTA
+static_assert(kSimtThreads - 2 * kChunk >= 128, "the row-normalising threads follow the cumsum threads");
 
 template <int K>
 struct SimtSmem {
@@ -105,11 +106,19 @@ kda_prefill_simt_kernel(PrefillArgs a)
             bs[r] = r < len ? a.beta[(t0 + r) * H + h] : 0.f;
         __syncthreads();
 
-        // in-chunk cumulative gate (exp2 space), one thread per key channel
+        // in-chunk cumulative gate (exp2 space), one thread per key channel; meanwhile the
+        // in-kernel L2 normalisation of the q and k rows, one thread per row
         if (tid < K) {
             float acc = 0.f;
             for (int r = 0; r < C; ++r) { acc += gam[r * KP + tid]; gam[r * KP + tid] = acc; }
             glast[tid] = acc;
+        } else if (tid >= kSimtThreads - 2 * C && (a.flags & kFlagQkL2Norm)) {
+            const int rr = tid - (kSimtThreads - 2 * C);
+            float *row = (rr < C ? qs : ks) + (rr % C) * KP;
+            float ss = 0.f;
+            for (int c = 0; c < K; ++c) ss += row[c] * row[c];
+            const float sc = rsqrtf(ss + kQkL2NormEps);
+            for (int c = 0; c < K; ++c) row[c] *= sc;
         }
         // T starts as the identity
         for (int i = tid; i < C * C; i += kSimtThreads) {

@@ -15,6 +15,11 @@ Contents
   type as a runner configuration, vllm.cpp PR #122, block B3, kda_state_dtype): the
   fp64 step of ``decode`` on the stored values, the output from the unrounded updated
   state, each updated slot then rounded to the nearest bf16 (``round_to_bf16``).
+* ``l2_normalize``: the in-kernel query/key normalisation option, x / sqrt(sum x^2 +
+  1e-6) over the key dimension in fp64 (the normalisation of the fused prologue that
+  the prompt path of vllm.cpp PR #110 names, chunk_kda_with_fused_gate; its epsilon is
+  not on the pages and is read as 1e-6); ``prefill`` / ``decode`` apply it to q and k
+  first when ``qk_l2norm`` is set.
 * ``chunked.prefill_chunked``: a second statement of the same definition, evaluated
   chunk by chunk (numpy, fp64), used to pin the chunk algebra that a chunked
   implementation relies on.
@@ -96,15 +101,27 @@ def default_threads() -> int:
         return max(1, os.cpu_count() or 1)
 
 
+QK_L2NORM_EPS = 1e-6
+
+
+def l2_normalize(x) -> np.ndarray:
+    """x / sqrt(sum over the last axis of x^2 + 1e-6), in fp64."""
+    x = _f64(x)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + QK_L2NORM_EPS)
+
+
 def prefill(q, k, v, g, beta, scale: float, init_state=None, cu_seqlens=None,
-            nthreads: int | None = None):
+            nthreads: int | None = None, qk_l2norm: bool = False):
     """Token-by-token fp64 prefill.
 
     q, k, g: [T, H, K]; v: [T, H, V]; beta: [T, H]; init_state: [N, H, K, V] or
-    None (zeros); cu_seqlens: [N+1] or None (one sequence of length T).
+    None (zeros); cu_seqlens: [N+1] or None (one sequence of length T).  With
+    ``qk_l2norm`` the q and k rows are normalised first (``l2_normalize``).
     Returns (out [T, H, V], final_state [N, H, K, V]) as float64 arrays.
     """
     q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    if qk_l2norm:
+        q, k = l2_normalize(q), l2_normalize(k)
     T, H, K = q.shape
     V = v.shape[-1]
     assert k.shape == (T, H, K) and g.shape == (T, H, K)
@@ -125,13 +142,17 @@ def prefill(q, k, v, g, beta, scale: float, init_state=None, cu_seqlens=None,
     return out, final
 
 
-def decode(q, k, v, g, beta, scale: float, pool, state_idx, nthreads: int | None = None):
+def decode(q, k, v, g, beta, scale: float, pool, state_idx, nthreads: int | None = None,
+           qk_l2norm: bool = False):
     """One fp64 decode step for N sequences.
 
     q, k, g: [N, H, K]; v: [N, H, V]; beta: [N, H]; pool: [S, H, K, V] float64
-    numpy array, updated IN PLACE at the slots state_idx [N].  Returns out [N, H, V].
+    numpy array, updated IN PLACE at the slots state_idx [N].  With ``qk_l2norm`` the
+    q and k rows are normalised first.  Returns out [N, H, V].
     """
     q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    if qk_l2norm:
+        q, k = l2_normalize(q), l2_normalize(k)
     N, H, K = q.shape
     V = v.shape[-1]
     if not (isinstance(pool, np.ndarray) and pool.dtype == np.float64
@@ -163,7 +184,8 @@ def round_to_bf16(x) -> np.ndarray:
     return np.where(np.abs(y) >= 2.0 ** 128, np.copysign(np.inf, y), y)
 
 
-def decode_bf16_state(q, k, v, g, beta, scale: float, pool, state_idx, nthreads: int | None = None):
+def decode_bf16_state(q, k, v, g, beta, scale: float, pool, state_idx, nthreads: int | None = None,
+                      qk_l2norm: bool = False):
     """One decode step on a pool stored in bf16.
 
     pool: [S, H, K, V] float64 numpy array holding bf16 values, updated IN PLACE at the
@@ -171,7 +193,7 @@ def decode_bf16_state(q, k, v, g, beta, scale: float, pool, state_idx, nthreads:
     the nearest bf16.  The output is read from the unrounded updated state.  Returns
     out [N, H, V].
     """
-    out = decode(q, k, v, g, beta, scale, pool, state_idx, nthreads)
+    out = decode(q, k, v, g, beta, scale, pool, state_idx, nthreads, qk_l2norm)
     for s in np.unique(_i64(state_idx)):
         pool[s] = round_to_bf16(pool[s])
     return out

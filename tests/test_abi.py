@@ -76,7 +76,7 @@ def _prefill(native, **kw):
     return native.lib.kda_chunk_prefill(
         vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
         vp(a["init"]), vp(a["cu"]), vp(a["out"]), vp(a["final"]), a["T"], a["N"], a["H"],
-        a["K"], a["V"], a["dtype"], a["out_dtype"], None)
+        a["K"], a["V"], a["dtype"], a["out_dtype"], a.get("flags", 0), None)
 
 
 def _decode(native, **kw):
@@ -88,7 +88,16 @@ def _decode(native, **kw):
     return native.lib.kda_recurrent_decode(
         vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
         vp(a["pool"]), vp(a["idx"]), vp(a["out"]), a["N"], a["S"], a["H"], a["K"], a["V"],
-        a["dtype"], a["out_dtype"], None)
+        a["dtype"], a["out_dtype"], a.get("flags", 0), None)
+
+
+def test_unknown_option_bits_are_rejected(native):
+    # every call is built to fail on its flags alone (sizes and addresses are valid)
+    assert _prefill(native, flags=2) == native.KDA_ERR_INVALID_ARG
+    assert _prefill(native, flags=native.KDA_FLAG_QK_L2NORM | 8) == native.KDA_ERR_INVALID_ARG
+    assert _decode(native, flags=4) == native.KDA_ERR_INVALID_ARG
+    assert _decode_bf16_state(native, flags=-1) == native.KDA_ERR_INVALID_ARG
+    assert _prefill_paged(native, flags=16) == native.KDA_ERR_INVALID_ARG
 
 
 def test_prefill_argument_validation(native):
@@ -134,7 +143,7 @@ def _prefill_paged(native, **kw):
     return native.lib.kda_chunk_prefill_paged(
         vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
         vp(a["pool"]), vp(a["idx"]), vp(a["cu"]), vp(a["out"]), a["T"], a["N"], a["S"], a["H"],
-        a["K"], a["V"], a["dtype"], a["out_dtype"], None)
+        a["K"], a["V"], a["dtype"], a["out_dtype"], a.get("flags", 0), None)
 
 
 def test_paged_prefill_validation_and_alias(native):
@@ -169,7 +178,7 @@ def _decode_bf16_state(native, **kw):
     return native.lib.kda_recurrent_decode_bf16_state(
         vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
         vp(a["pool"]), vp(a["idx"]), vp(a["out"]), a["N"], a["S"], a["H"], a["K"], a["V"],
-        a["dtype"], a["out_dtype"], None)
+        a["dtype"], a["out_dtype"], a.get("flags", 0), None)
 
 
 def test_decode_bf16_state_argument_validation_and_alias(native):
@@ -210,7 +219,7 @@ def _prefill_ws(native, ws, ws_bytes, **kw):
     return native.lib.kda_chunk_prefill_ws(
         vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
         vp(a["init"]), vp(a["cu"]), vp(a["out"]), vp(a["final"]), a["T"], a["N"], a["H"],
-        a["K"], a["V"], a["dtype"], a["out_dtype"], vp(ws), ws_bytes, None)
+        a["K"], a["V"], a["dtype"], a["out_dtype"], vp(ws), ws_bytes, a.get("flags", 0), None)
 
 
 def test_workspace_query_is_zero_without_the_tensor_core_kernel(native):
@@ -277,7 +286,7 @@ def test_paged_prefill_ws_validation_and_alias(native):
         return native.lib.kda_chunk_prefill_paged_ws(
             vp(a["q"]), vp(a["k"]), vp(a["v"]), vp(a["g"]), vp(a["beta"]), a["scale"],
             vp(a["pool"]), vp(a["idx"]), vp(a["cu"]), vp(a["out"]), a["T"], a["N"], a["S"],
-            a["H"], a["K"], a["V"], a["dtype"], a["out_dtype"], vp(ws), ws_bytes, None)
+            a["H"], a["K"], a["V"], a["dtype"], a["out_dtype"], vp(ws), ws_bytes, a.get("flags", 0), None)
 
     ws = BASE + (1 << 36)
     assert call(ws, need, idx=None) == native.KDA_ERR_INVALID_ARG
