@@ -7,8 +7,11 @@ returned): one ``kda_chunk_prefill_ws`` call (the 4-CTA cluster kernel that shar
 chunk's operands across the value tiles).  ``value`` is prefill tokens/s.  The same run
 also times the varlen packed workload (8 sequences, lengths U[256, 8192], nonzero
 initial states) under "prefill_varlen", the long prompt (T=65536) under "prefill_long",
-and the paged-decode workload (256 sequences x 1 token, H=32, K=V=128, 1024-slot fp32
-pool, 64 steps carrying state in place) under "decode" / "decode_bf16_state".
+the paged-decode workload (256 sequences x 1 token, H=32, K=V=128, 1024-slot fp32
+pool, 64 steps carrying state in place) under "decode" / "decode_bf16_state", and the
+causal convolution in front of the op (width 4, SiLU, taps in paged slots) on the
+varlen workload's 12,288 [q|k|v] channels ("conv_prefill") and on one token of 256
+sequences ("conv_update").
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--only all|prefill|decode] [--decode-seqs S]
@@ -396,8 +399,60 @@ def run_ours(args):
                          "achieved": round(d_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                          "frac": round(d_gbs / peak_hbm, 4),
                          "traffic": traffic.get("decode_bf16_state_paged")}}
+    if args.only in ("all", "conv"):
+        blocks, n_launch = measure_conv(args, dev, stream, flush, peak_hbm, traffic)
+        line.update(blocks)
+        launches += n_launch
     line["gpu_launches"] = launches
     print(json.dumps(line), flush=True)
+
+
+def conv_bytes(case, prompt):
+    """Algorithmic HBM bytes of one causal-convolution call: inputs read and outputs
+    written once (bf16), the carried taps of every sequence read and written, the fp32
+    weights and bias read."""
+    T, D = case.x.shape
+    W = case.weight.shape[1]
+    es = case.x.element_size()
+    N = case.state_idx.numel()
+    return T * D * es * 2 + N * (W - 1) * D * es * 2 + D * (W + 1) * 4
+
+
+def measure_conv(args, dev, stream, flush, peak_hbm, traffic):
+    """The causal convolution in front of the op: the prompt pass on the varlen packed
+    workload's [q|k|v] channels and the one-token update of the paged-decode workload
+    (width 4, SiLU, taps carried in paged slots)."""
+    import torch
+    from kimi_delta_attention_09_gb300 import _native, inputs
+    out_blocks, n_launch = {}, 0
+    for key, make, prompt, tkey in (("conv_prefill", inputs.conv_varlen, True, "conv_fwd_varlen"),
+                                    ("conv_update", inputs.conv_decode, False, "conv_update_decode")):
+        c = make()
+        x, w, b = c.x.to(dev), c.weight.to(dev), c.bias.to(dev)
+        st, idx, cu = c.conv_state.to(dev), c.state_idx.to(dev), c.cu_seqlens.to(dev)
+        out = torch.empty_like(x)
+
+        if prompt:
+            def step():
+                _native.kda_causal_conv1d_fwd(x, w, b, st, idx, cu, out, _native.KDA_CONV_ACT_SILU, stream)
+        else:
+            def step():
+                _native.kda_causal_conv1d_update(x, w, b, st, idx, out, _native.KDA_CONV_ACT_SILU, stream)
+
+        n = max(3, min(args.steps, 20))
+        times = time_steps(step, n, args.warmup, stream, flush)
+        n_launch += n * (2 if prompt else 1)
+        ms = statistics.mean(times)
+        nbytes = conv_bytes(c, prompt)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out_blocks[key] = {
+            "workload": c.name, "metric": "GB/s", "value": round(gbs, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "steps": n, "algorithmic_bytes": nbytes,
+            "roofline": {"bound": "hbm", "kernel": "kda_conv_fwd_kernel" if prompt else "kda_conv_update_kernel",
+                         "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                         "frac": round(gbs / peak_hbm, 4), "traffic": traffic.get(tkey)}}
+        del c, x, w, b, st, idx, cu, out
+    return out_blocks, n_launch
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -472,7 +527,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all")
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "conv"], default="all")
     ap.add_argument("--decode-seqs", type=int, default=256)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)          # at least 3 untimed warm-up steps

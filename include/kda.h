@@ -25,6 +25,9 @@
  *                            paged pool slot, updated in place (state slots keyed
  *                            by per-sequence indices, PR #122 block B2); its
  *                            _bf16_state form keeps the pool in bf16.
+ *   kda_causal_conv1d_fwd / _update -- the short causal convolution in front of the
+ *                            op over the packed [q|k|v] channels, its taps carried per
+ *                            slot (PR #122 block B2; PR #113 commit body).
  *
  * Conventions for every call
  * --------------------------
@@ -353,6 +356,67 @@ KDA_API int kda_recurrent_decode_bf16_state(const void *q, const void *k, const 
                                             int32_t num_seqs, int32_t num_slots, int32_t num_heads,
                                             int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
                                             int32_t out_dtype, int32_t flags, void *stream);
+
+/* Activation of the causal convolution. */
+enum kda_conv_activation {
+    KDA_CONV_ACT_NONE = 0,
+    KDA_CONV_ACT_SILU = 1      /* z / (1 + exp(-z)) */
+};
+
+/*
+ * The short causal convolution in front of the KDA op, over a packed prompt.
+ *
+ * Defined by the conv taps of the KDA block (vllm.cpp PR #122 "fold Kimi-Linear onto the
+ * shared paged runner", block B2: CausalConv1dFwd over the varlen prompt, the carried
+ * conv_state split as chunk(3) into [q|k|v]; vllm.cpp PR #113, commit body: the conv-tap
+ * carry of the decode regime).  A depthwise convolution of width W over D channels (the
+ * packed [q|k|v] projections): per sequence n and channel c, with the W - 1 taps carried
+ * in slot state_idx[n] prepended to the sequence's inputs (oldest first),
+ *     out_t = act(bias_c + sum_{j < W} weight[c][j] xe_{t+j})
+ * so out_t sees x_t and the W - 1 inputs before it; afterwards the slot holds the last
+ * W - 1 entries of [taps | inputs] (exact copies of inputs: a prompt split anywhere and
+ * continued from its taps gives the unsplit result bit for bit).
+ *
+ *   x           [total_tokens, D]   dtype       inputs, packed by cu_seqlens
+ *   weight      [D, W]              fp32        per-channel taps, weight[c][W-1] on x_t
+ *   bias        [D]                 fp32        or NULL
+ *   conv_state  [num_slots, W-1, D] dtype       carried taps, read and updated IN PLACE at
+ *                                               the selected slots (every other slot is
+ *                                               left bit-identical); NULL: zero taps,
+ *                                               nothing kept.  A fresh prompt starts from
+ *                                               a zeroed slot.
+ *   state_idx   [num_seqs]          int32       slot of each sequence (with conv_state);
+ *                                               read on the device; distinct (duplicates
+ *                                               race); an index outside [0, num_slots)
+ *                                               gives zero taps and keeps nothing
+ *   cu_seqlens  [num_seqs + 1]      int32       non-decreasing sequence bounds (read on
+ *                                               the device and clamped to [0, total_tokens])
+ *   out         [total_tokens, D]   out_dtype   rows outside every sequence are not written
+ *   D >= 4 and a multiple of 4; W in 1..4; activation a kda_conv_activation.
+ * Pointers 16-byte aligned; out must not overlap any input, conv_state no input or out
+ * (KDA_ERR_ALIAS).  Two kernels on `stream`: the outputs (reading the old taps), then the
+ * new taps.
+ */
+KDA_API int kda_causal_conv1d_fwd(const void *x, const float *weight, const float *bias,
+                                  void *conv_state, const int32_t *state_idx,
+                                  const int32_t *cu_seqlens, void *out, int64_t total_tokens,
+                                  int32_t num_seqs, int32_t num_slots, int32_t dim,
+                                  int32_t width, int32_t dtype, int32_t out_dtype,
+                                  int32_t activation, void *stream);
+
+/*
+ * One token per sequence through the same convolution, the taps of slot state_idx[n]
+ * shifted by one in place (vllm.cpp PR #122, block B2: CausalConv1dUpdate for decode).
+ *
+ *   x    [num_seqs, D] dtype;   out [num_seqs, D] out_dtype;   every other argument as for
+ *   kda_causal_conv1d_fwd.  One kernel on `stream`; a decode step after
+ *   kda_causal_conv1d_fwd on the same slot continues the prompt exactly.
+ */
+KDA_API int kda_causal_conv1d_update(const void *x, const float *weight, const float *bias,
+                                     void *conv_state, const int32_t *state_idx, void *out,
+                                     int32_t num_seqs, int32_t num_slots, int32_t dim,
+                                     int32_t width, int32_t dtype, int32_t out_dtype,
+                                     int32_t activation, void *stream);
 
 #ifdef __cplusplus
 }

@@ -21,13 +21,16 @@ KDA_ERR_TIMEOUT = -5
 KDA_DTYPE_F32 = 0
 KDA_DTYPE_BF16 = 1
 KDA_FLAG_QK_L2NORM = 1
+KDA_CONV_ACT_NONE = 0
+KDA_CONV_ACT_SILU = 1
 ABI_VERSION = 4
 
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
             "kda_chunk_prefill", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_ws",
             "kda_chunk_prefill_noalloc", "kda_chunk_prefill_paged_ws",
             "kda_chunk_prefill_paged", "kda_chunk_prefill_status", "kda_set_prefill_wait_limit",
-            "kda_recurrent_decode", "kda_recurrent_decode_bf16_state")
+            "kda_recurrent_decode", "kda_recurrent_decode_bf16_state", "kda_causal_conv1d_fwd",
+            "kda_causal_conv1d_update")
 
 
 class KdaError(RuntimeError):
@@ -77,6 +80,12 @@ def _load() -> ctypes.CDLL:
     lib.kda_recurrent_decode_bf16_state.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp,
                                                     i32, i32, i32, i32, i32, i32, i32, i32, vp]
     lib.kda_recurrent_decode_bf16_state.restype = ctypes.c_int
+    lib.kda_causal_conv1d_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32,
+                                          i32, i32, i32, vp]
+    lib.kda_causal_conv1d_fwd.restype = ctypes.c_int
+    lib.kda_causal_conv1d_update.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                             i32, vp]
+    lib.kda_causal_conv1d_update.restype = ctypes.c_int
     if lib.kda_abi_version() != ABI_VERSION:
         raise RuntimeError(f"libkda.so ABI {lib.kda_abi_version()} != expected {ABI_VERSION}")
     return lib
@@ -338,3 +347,49 @@ def kda_recurrent_decode_bf16_state(q, k, v, g, beta, scale, state_pool, state_i
     import torch
     _decode("kda_recurrent_decode_bf16_state", q, k, v, g, beta, scale, state_pool, state_idx, out,
             torch.bfloat16, stream, flags)
+
+
+def _conv_checks(x, weight, bias, conv_state, state_idx, out):
+    import torch
+    for name, t in (("x", x), ("weight", weight), ("bias", bias), ("conv_state", conv_state),
+                    ("state_idx", state_idx), ("out", out)):
+        if t is not None:
+            _need(t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CUDA tensor")
+    D, W = weight.shape
+    _need(weight.dtype == torch.float32, "weight must be fp32 [D, W]")
+    _need(x.shape[-1] == D and out.shape == x.shape, "x, out must be [rows, D]")
+    _need(bias is None or (bias.dtype == torch.float32 and bias.shape == (D,)), "bias must be fp32 [D]")
+    if conv_state is not None:
+        _need(conv_state.dtype == x.dtype and tuple(conv_state.shape[1:]) == (W - 1, D),
+              "conv_state must be [S, W - 1, D] of x's dtype")
+        _need(state_idx is not None and state_idx.dtype == torch.int32, "state_idx must be int32 [N]")
+    return D, W
+
+
+def kda_causal_conv1d_fwd(x, weight, bias, conv_state, state_idx, cu_seqlens, out,
+                          activation=KDA_CONV_ACT_NONE, stream=None) -> None:
+    """Enqueue ``kda_causal_conv1d_fwd``: x [T, D], weight [D, W] fp32, bias [D] or None,
+    conv_state [S, W - 1, D] (x's dtype, updated in place) or None, state_idx [N] int32,
+    cu_seqlens [N + 1] int32, out [T, D] (its dtype selects the output element type)."""
+    import torch
+    D, W = _conv_checks(x, weight, bias, conv_state, state_idx, out)
+    _need(cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32, "cu_seqlens must be int32 on CUDA")
+    N = cu_seqlens.numel() - 1
+    S = 0 if conv_state is None else conv_state.shape[0]
+    rc = lib.kda_causal_conv1d_fwd(_ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state),
+                                   _ptr(state_idx), _ptr(cu_seqlens), _ptr(out), x.shape[0], N, S,
+                                   D, W, _dtype_code(x), _dtype_code(out), int(activation),
+                                   _stream_handle(stream))
+    _check("kda_causal_conv1d_fwd", rc)
+
+
+def kda_causal_conv1d_update(x, weight, bias, conv_state, state_idx, out,
+                             activation=KDA_CONV_ACT_NONE, stream=None) -> None:
+    """Enqueue ``kda_causal_conv1d_update``: one token per sequence, x [N, D]."""
+    D, W = _conv_checks(x, weight, bias, conv_state, state_idx, out)
+    S = 0 if conv_state is None else conv_state.shape[0]
+    rc = lib.kda_causal_conv1d_update(_ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state),
+                                      _ptr(state_idx), _ptr(out), x.shape[0], S, D, W,
+                                      _dtype_code(x), _dtype_code(out), int(activation),
+                                      _stream_handle(stream))
+    _check("kda_causal_conv1d_update", rc)

@@ -409,4 +409,63 @@ int kda_recurrent_decode_bf16_state(const void *q, const void *k, const void *v,
                             out_dtype, flags, stream);
 }
 
+static int causal_conv(bool prompt, const void *x, const float *weight, const float *bias,
+                       void *conv_state, const int32_t *state_idx, const int32_t *cu_seqlens,
+                       void *out, int64_t total_tokens, int32_t num_seqs, int32_t num_slots,
+                       int32_t dim, int32_t width, int32_t dtype, int32_t out_dtype,
+                       int32_t activation, void *stream)
+{
+    if (total_tokens < 0 || num_seqs < 0 || num_slots < 0 || dim < 4 || (dim & 3) != 0 ||
+        width < 1 || width > 4 || (activation != KDA_CONV_ACT_NONE && activation != KDA_CONV_ACT_SILU))
+        return KDA_ERR_INVALID_ARG;
+    if (!dtype_supported(dtype) || !dtype_supported(out_dtype)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return KDA_OK;
+    const int64_t rows = prompt ? total_tokens : num_seqs;
+    if (prompt && (!cu_seqlens || !aligned16(cu_seqlens))) return KDA_ERR_INVALID_ARG;
+    if (rows > 0 && (!x || !aligned16(x) || !out || !aligned16(out))) return KDA_ERR_INVALID_ARG;
+    if (!weight || !aligned16(weight) || (bias && !aligned16(bias))) return KDA_ERR_INVALID_ARG;
+    if (conv_state && (!aligned16(conv_state) || !state_idx || !aligned16(state_idx)))
+        return KDA_ERR_INVALID_ARG;
+
+    const uint64_t D = (uint64_t)dim, W = (uint64_t)width;
+    const uint64_t es = dtype == KDA_DTYPE_BF16 ? 2 : 4, eo = out_dtype == KDA_DTYPE_BF16 ? 2 : 4;
+    const Range in[] = {{x, (uint64_t)rows * D * es}, {weight, D * W * 4}, {bias, D * 4},
+                        {state_idx, conv_state ? (uint64_t)num_seqs * 4 : 0},
+                        {cu_seqlens, prompt ? ((uint64_t)num_seqs + 1) * 4 : 0}};
+    const Range r_out{out, (uint64_t)rows * D * eo};
+    const Range r_state{conv_state, (uint64_t)num_slots * (W - 1) * D * es};
+    for (const Range &r : in)
+        if (overlaps(r_out, r) || overlaps(r_state, r)) return KDA_ERR_ALIAS;
+    if (overlaps(r_out, r_state)) return KDA_ERR_ALIAS;
+
+    kda::ConvArgs a{};
+    a.x = x; a.weight = weight; a.bias = bias; a.state = conv_state; a.state_idx = state_idx;
+    a.cu_seqlens = cu_seqlens; a.out = out; a.total_tokens = prompt ? total_tokens : num_seqs;
+    a.num_seqs = num_seqs; a.num_slots = num_slots; a.dim = dim; a.width = width;
+    a.dtype = dtype; a.out_dtype = out_dtype; a.activation = activation;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return finish(prompt ? kda::launch_conv_fwd(a, st) : kda::launch_conv_update(a, st));
+}
+
+int kda_causal_conv1d_fwd(const void *x, const float *weight, const float *bias,
+                          void *conv_state, const int32_t *state_idx,
+                          const int32_t *cu_seqlens, void *out, int64_t total_tokens,
+                          int32_t num_seqs, int32_t num_slots, int32_t dim,
+                          int32_t width, int32_t dtype, int32_t out_dtype,
+                          int32_t activation, void *stream)
+{
+    return causal_conv(true, x, weight, bias, conv_state, state_idx, cu_seqlens, out, total_tokens,
+                       num_seqs, num_slots, dim, width, dtype, out_dtype, activation, stream);
+}
+
+int kda_causal_conv1d_update(const void *x, const float *weight, const float *bias,
+                             void *conv_state, const int32_t *state_idx, void *out,
+                             int32_t num_seqs, int32_t num_slots, int32_t dim,
+                             int32_t width, int32_t dtype, int32_t out_dtype,
+                             int32_t activation, void *stream)
+{
+    return causal_conv(false, x, weight, bias, conv_state, state_idx, nullptr, out, 0, num_seqs,
+                       num_slots, dim, width, dtype, out_dtype, activation, stream);
+}
+
 }  // extern "C"

@@ -83,6 +83,21 @@ cudaError_t launch_prefill_rr(const PrefillArgs &a, void *workspace, size_t work
 // limit of every wait inside the prefill kernel (0: the default of 2 s)
 void set_prefill_wait_limit_ns(unsigned long long ns);
 
+// The short causal convolution over packed channels with carried taps.
+constexpr int kConvActNone = 0, kConvActSilu = 1;
+struct ConvArgs {
+    const void *x;                // [T, D] (prompt) or [N, D] (decode), dtype
+    const float *weight, *bias;   // [D, W], [D] or nullptr
+    void *state;                  // [S, W - 1, D] dtype, or nullptr (zero taps, nothing kept)
+    const int32_t *state_idx;     // [N] (with state)
+    const int32_t *cu_seqlens;    // [N + 1] (prompt)
+    void *out;                    // like x, out_dtype
+    int64_t total_tokens;
+    int32_t num_seqs, num_slots, dim, width, dtype, out_dtype, activation;
+};
+cudaError_t launch_conv_fwd(const ConvArgs &a, cudaStream_t stream);
+cudaError_t launch_conv_update(const ConvArgs &a, cudaStream_t stream);
+
 // One-token paged decode.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 

@@ -180,6 +180,54 @@ def _prefill_after_lengths(gen, lengths, H, K, V, dtype, init_std, seed, name):
                        cu_seqlens=cu, init_state=init, scale=K ** -0.5)
 
 
+@dataclass
+class ConvCase:
+    name: str
+    seed: int
+    x: torch.Tensor            # [T, D]  dtype (the packed [q|k|v] channels)
+    weight: torch.Tensor       # [D, W]  fp32
+    bias: torch.Tensor         # [D]     fp32
+    conv_state: torch.Tensor   # [S, W-1, D] dtype (carried taps per slot)
+    state_idx: torch.Tensor    # [N] int32, distinct slots
+    cu_seqlens: torch.Tensor   # [N+1] int32
+
+
+def conv_case(lengths, D: int, W: int, dtype: str = "bf16", seed: int = 0, slots: int = 0,
+              name: str = "custom_conv") -> ConvCase:
+    """Causal-conv inputs: x ~ N(0, 1); weight ~ N(0, 1 / W); bias ~ N(0, 0.1^2); a pool
+    of max(slots, N) carried-tap slots ~ N(0, 1); N distinct slots drawn by permutation.
+    Draw order: x, weight, bias, taps, slot permutation."""
+    gen = torch.Generator().manual_seed(seed)
+    lengths = [int(x) for x in lengths]
+    cu = torch.zeros(len(lengths) + 1, dtype=torch.int32)
+    if lengths:
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    T = int(cu[-1])
+    S = max(slots, len(lengths))
+    x = torch.randn(T, D, generator=gen).to(DTYPES[dtype]).contiguous()
+    weight = (torch.randn(D, W, generator=gen) / W ** 0.5).float().contiguous()
+    bias = (torch.randn(D, generator=gen) * 0.1).float().contiguous()
+    state = torch.randn(S, max(W - 1, 0), D, generator=gen).to(DTYPES[dtype]).contiguous()
+    idx = torch.randperm(S, generator=gen)[:len(lengths)].to(torch.int32)
+    return ConvCase(name=name, seed=seed, x=x, weight=weight, bias=bias, conv_state=state,
+                    state_idx=idx, cu_seqlens=cu)
+
+
+def conv_varlen(W: int = 4) -> ConvCase:
+    """The varlen packed workload's lengths (8 sequences, U[256, 8192], seed 2) over its
+    [q|k|v] channels (3 x 32 heads x 128 = 12,288), taps carried in 8 slots, width 4."""
+    gen = torch.Generator().manual_seed(2)
+    lengths = [int(x) for x in torch.randint(256, 8192 + 1, (8,), generator=gen)]
+    return conv_case(lengths, D=3 * 32 * 128, W=W, dtype="bf16", seed=5, slots=8,
+                     name=f"conv_varlen_N8_D12288_W{W}_bf16")
+
+
+def conv_decode(W: int = 4) -> ConvCase:
+    """One token for each of 256 sequences over 12,288 channels, taps in 1024 slots."""
+    return conv_case([1] * 256, D=3 * 32 * 128, W=W, dtype="bf16", seed=6, slots=1024,
+                     name=f"conv_decode_N256_S1024_D12288_W{W}_bf16")
+
+
 WORKLOADS = {
     "tiny_f32": tiny_f32,
     "single_prompt": single_prompt,

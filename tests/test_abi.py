@@ -296,3 +296,36 @@ def test_paged_prefill_ws_validation_and_alias(native):
     assert call(BASE + (1 << 32) + 64, need) == native.KDA_ERR_ALIAS         # workspace over the pool
     assert call(BASE + (5 << 24), need) == native.KDA_ERR_ALIAS              # ... over state_idx
     assert call(None, 0, N=0) == native.KDA_OK
+
+
+def _conv(native, prompt=True, **kw):
+    vp = ctypes.c_void_p
+    a = dict(x=BASE, w=BASE + (1 << 24), b=BASE + (2 << 24), st=BASE + (3 << 24), idx=BASE + (4 << 24),
+             cu=BASE + (5 << 24), out=BASE + (6 << 24), T=100, N=2, S=4, D=64, W=4, dtype=1,
+             out_dtype=0, act=1)
+    a.update(kw)
+    if prompt:
+        return native.lib.kda_causal_conv1d_fwd(
+            vp(a["x"]), vp(a["w"]), vp(a["b"]), vp(a["st"]), vp(a["idx"]), vp(a["cu"]), vp(a["out"]),
+            a["T"], a["N"], a["S"], a["D"], a["W"], a["dtype"], a["out_dtype"], a["act"], None)
+    return native.lib.kda_causal_conv1d_update(
+        vp(a["x"]), vp(a["w"]), vp(a["b"]), vp(a["st"]), vp(a["idx"]), vp(a["out"]),
+        a["N"], a["S"], a["D"], a["W"], a["dtype"], a["out_dtype"], a["act"], None)
+
+
+def test_conv_validation_and_alias(native):
+    for prompt in (True, False):
+        assert _conv(native, prompt, W=0) == native.KDA_ERR_INVALID_ARG
+        assert _conv(native, prompt, W=5) == native.KDA_ERR_INVALID_ARG
+        assert _conv(native, prompt, D=66) == native.KDA_ERR_INVALID_ARG      # not a multiple of 4
+        assert _conv(native, prompt, act=2) == native.KDA_ERR_INVALID_ARG
+        assert _conv(native, prompt, dtype=7) == native.KDA_ERR_UNSUPPORTED
+        assert _conv(native, prompt, x=None) == native.KDA_ERR_INVALID_ARG
+        assert _conv(native, prompt, w=None) == native.KDA_ERR_INVALID_ARG
+        assert _conv(native, prompt, idx=None) == native.KDA_ERR_INVALID_ARG  # taps need slots
+        assert _conv(native, prompt, out=BASE + 8) == native.KDA_ERR_INVALID_ARG   # misaligned
+        assert _conv(native, prompt, N=0) == native.KDA_OK
+        assert _conv(native, prompt, out=BASE + 64) == native.KDA_ERR_ALIAS    # out over x
+        assert _conv(native, prompt, st=BASE + (6 << 24) + 16) == native.KDA_ERR_ALIAS   # taps over out
+        assert _conv(native, prompt, st=BASE + (1 << 24) - 64) == native.KDA_ERR_ALIAS   # taps over weight
+    assert _conv(native, True, cu=None) == native.KDA_ERR_INVALID_ARG
