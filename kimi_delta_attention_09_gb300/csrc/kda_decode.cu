@@ -37,7 +37,7 @@ namespace {
 constexpr int kDecThreads = 128;
 constexpr int kDecCols = 32;   // V columns per CTA
 
-template <typename Tin, typename Tout, int K, int V>
+template <typename Tin, typename Tout, int K, int V, bool kL2>
 __global__ void __launch_bounds__(kDecThreads)
 kda_decode_kernel(DecodeArgs a)
 {
@@ -94,8 +94,10 @@ kda_decode_kernel(DecodeArgs a)
         pq[0] += s[j].x * qr[j]; pq[1] += s[j].y * qr[j];
         pq[2] += s[j].z * qr[j]; pq[3] += s[j].w * qr[j];
         kq += kr[j] * qr[j];
-        kk += kr[j] * kr[j];
-        qq += qr[j] * qr[j];
+        if (kL2) {
+            kk += kr[j] * kr[j];
+            qq += qr[j] * qr[j];
+        }
     }
     // reduce over the 4 row groups of this warp (lanes differing in bits 3, 4)
 #pragma unroll
@@ -106,18 +108,22 @@ kda_decode_kernel(DecodeArgs a)
             pq[i] += __shfl_xor_sync(0xffffffffu, pq[i], off);
         }
         kq += __shfl_xor_sync(0xffffffffu, kq, off);
-        kk += __shfl_xor_sync(0xffffffffu, kk, off);
-        qq += __shfl_xor_sync(0xffffffffu, qq, off);
+        if (kL2) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            qq += __shfl_xor_sync(0xffffffffu, qq, off);
+        }
     }
     // ... and over the 4 warps
-    __shared__ float red[kDecThreads / 32][8][11];
+    __shared__ float red[kDecThreads / 32][8][kL2 ? 11 : 9];
     const int warp = tid >> 5, lane = tid & 31;
     if (lane < 8) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) { red[warp][lane][i] = pk[i]; red[warp][lane][4 + i] = pq[i]; }
         red[warp][lane][8] = kq;
-        red[warp][lane][9] = kk;
-        red[warp][lane][10] = qq;
+        if (kL2) {
+            red[warp][lane][9] = kk;
+            red[warp][lane][10] = qq;
+        }
     }
     __syncthreads();
     float u[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
@@ -127,17 +133,19 @@ kda_decode_kernel(DecodeArgs a)
 #pragma unroll
         for (int i = 0; i < 4; ++i) { u[i] += red[w][cg][i]; qs[i] += red[w][cg][4 + i]; }
         kq += red[w][cg][8];
-        kk += red[w][cg][9];
-        qq += red[w][cg][10];
+        if (kL2) {
+            kk += red[w][cg][9];
+            qq += red[w][cg][10];
+        }
     }
-    // in-kernel L2 normalisation: every product above is linear in k and in q
-    const float rk = (a.flags & kFlagQkL2Norm) ? rsqrtf(kk + kQkL2NormEps) : 1.f;
-    const float rq = (a.flags & kFlagQkL2Norm) ? rsqrtf(qq + kQkL2NormEps) : 1.f;
+    if (kL2) {   // in-kernel L2 normalisation: every product above is linear in k and in q
+        const float rk = rsqrtf(kk + kQkL2NormEps), rq = rsqrtf(qq + kQkL2NormEps);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) { u[i] *= rk; qs[i] *= rq; }
-    kq *= rk * rq;
+        for (int i = 0; i < 4; ++i) { u[i] *= rk; qs[i] *= rq; }
+        kq *= rk * rq;
 #pragma unroll
-    for (int j = 0; j < kRowsPerThread; ++j) kr[j] *= rk;
+        for (int j = 0; j < kRowsPerThread; ++j) kr[j] *= rk;
+    }
 
     const float beta = a.beta[n * H + h];
     const Tin *vp = static_cast<const Tin *>(a.v) + (n * H + h) * V + col0;
@@ -163,7 +171,7 @@ constexpr int kDecCols16 = 64;   // V columns per CTA on a bf16 pool
 // The same step on a bf16 pool: thread t owns columns [8 (t % 8), +8) of the CTA's
 // 64 on rows t / 8 + 16 j; the state is widened to fp32 on load and rounded to
 // nearest-even bf16 on store.
-template <typename Tin, typename Tout, int K, int V>
+template <typename Tin, typename Tout, int K, int V, bool kL2>
 __global__ void __launch_bounds__(kDecThreads, 5)
 kda_decode_bf16_state_kernel(DecodeArgs a)
 {
@@ -227,8 +235,10 @@ kda_decode_bf16_state_kernel(DecodeArgs a)
 #pragma unroll
         for (int i = 0; i < 8; ++i) { pk[i] += x[i] * kr[j]; pq[i] += x[i] * qr[j]; }
         kq += kr[j] * qr[j];
-        kk += kr[j] * kr[j];
-        qq += qr[j] * qr[j];
+        if (kL2) {
+            kk += kr[j] * kr[j];
+            qq += qr[j] * qr[j];
+        }
     }
 #pragma unroll
     for (int off = 8; off <= 16; off <<= 1) {
@@ -238,17 +248,21 @@ kda_decode_bf16_state_kernel(DecodeArgs a)
             pq[i] += __shfl_xor_sync(0xffffffffu, pq[i], off);
         }
         kq += __shfl_xor_sync(0xffffffffu, kq, off);
-        kk += __shfl_xor_sync(0xffffffffu, kk, off);
-        qq += __shfl_xor_sync(0xffffffffu, qq, off);
+        if (kL2) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            qq += __shfl_xor_sync(0xffffffffu, qq, off);
+        }
     }
-    __shared__ float red[kDecThreads / 32][8][19];
+    __shared__ float red[kDecThreads / 32][8][kL2 ? 19 : 17];
     const int warp = tid >> 5, lane = tid & 31;
     if (lane < 8) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) { red[warp][lane][i] = pk[i]; red[warp][lane][8 + i] = pq[i]; }
         red[warp][lane][16] = kq;
-        red[warp][lane][17] = kk;
-        red[warp][lane][18] = qq;
+        if (kL2) {
+            red[warp][lane][17] = kk;
+            red[warp][lane][18] = qq;
+        }
     }
     __syncthreads();
     float u[8], qs[8];
@@ -260,17 +274,19 @@ kda_decode_bf16_state_kernel(DecodeArgs a)
 #pragma unroll
         for (int i = 0; i < 8; ++i) { u[i] += red[w][cg][i]; qs[i] += red[w][cg][8 + i]; }
         kq += red[w][cg][16];
-        kk += red[w][cg][17];
-        qq += red[w][cg][18];
+        if (kL2) {
+            kk += red[w][cg][17];
+            qq += red[w][cg][18];
+        }
     }
-    // in-kernel L2 normalisation: every product above is linear in k and in q
-    const float rk = (a.flags & kFlagQkL2Norm) ? rsqrtf(kk + kQkL2NormEps) : 1.f;
-    const float rq = (a.flags & kFlagQkL2Norm) ? rsqrtf(qq + kQkL2NormEps) : 1.f;
+    if (kL2) {   // in-kernel L2 normalisation: every product above is linear in k and in q
+        const float rk = rsqrtf(kk + kQkL2NormEps), rq = rsqrtf(qq + kQkL2NormEps);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { u[i] *= rk; qs[i] *= rq; }
-    kq *= rk * rq;
+        for (int i = 0; i < 8; ++i) { u[i] *= rk; qs[i] *= rq; }
+        kq *= rk * rq;
 #pragma unroll
-    for (int j = 0; j < kRowsPerThread; ++j) kr[j] *= rk;
+        for (int j = 0; j < kRowsPerThread; ++j) kr[j] *= rk;
+    }
 
     const float beta = a.beta[n * H + h];
     const Tin *vp = static_cast<const Tin *>(a.v) + (n * H + h) * V + col0;
@@ -298,16 +314,23 @@ kda_decode_bf16_state_kernel(DecodeArgs a)
     }
 }
 
-template <typename Tin, typename Tout, int K, int V>
-cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream)
+template <typename Tin, typename Tout, int K, int V, bool kL2>
+void launch_decode_l2(const DecodeArgs &a, cudaStream_t stream)
 {
     if (a.state_dtype == kDtypeBF16) {
         dim3 grid((unsigned)((int64_t)a.num_seqs * (V / kDecCols16)), (unsigned)a.num_heads);
-        kda_decode_bf16_state_kernel<Tin, Tout, K, V><<<grid, kDecThreads, 0, stream>>>(a);
+        kda_decode_bf16_state_kernel<Tin, Tout, K, V, kL2><<<grid, kDecThreads, 0, stream>>>(a);
     } else {
         dim3 grid((unsigned)((int64_t)a.num_seqs * (V / kDecCols)), (unsigned)a.num_heads);
-        kda_decode_kernel<Tin, Tout, K, V><<<grid, kDecThreads, 0, stream>>>(a);
+        kda_decode_kernel<Tin, Tout, K, V, kL2><<<grid, kDecThreads, 0, stream>>>(a);
     }
+}
+
+template <typename Tin, typename Tout, int K, int V>
+cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t stream)
+{
+    if (a.flags & kFlagQkL2Norm) launch_decode_l2<Tin, Tout, K, V, true>(a, stream);
+    else launch_decode_l2<Tin, Tout, K, V, false>(a, stream);
     return cudaGetLastError();
 }
 

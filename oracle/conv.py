@@ -27,6 +27,12 @@ ACT_NONE = 0
 ACT_SILU = 1
 
 
+def _f64(x):
+    if hasattr(x, "detach"):  # a torch tensor on the CPU (any dtype)
+        x = x.detach().cpu().double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
 def _act(z, activation):
     if activation == ACT_SILU:
         return z / (1.0 + np.exp(-z))
@@ -37,10 +43,10 @@ def conv_prefill(x, weight, bias, conv_state, state_idx, cu_seqlens, activation=
     """x [T, D]; weight [D, W]; bias [D] or None; conv_state [S, W-1, D] float64 numpy
     array updated IN PLACE at the slots state_idx [N] (None: zero taps, nothing kept);
     cu_seqlens [N+1].  Returns y [T, D] float64 (rows outside every sequence are zero)."""
-    x = np.asarray(x, dtype=np.float64)
-    w = np.asarray(weight, dtype=np.float64)
+    x = _f64(x)
+    w = _f64(weight)
     D, W = w.shape
-    b = np.zeros(D) if bias is None else np.asarray(bias, dtype=np.float64)
+    b = np.zeros(D) if bias is None else _f64(bias)
     cu = [int(c) for c in cu_seqlens]
     y = np.zeros_like(x)
     for n in range(len(cu) - 1):
@@ -63,7 +69,7 @@ def conv_prefill(x, weight, bias, conv_state, state_idx, cu_seqlens, activation=
 def conv_update(x, weight, bias, conv_state, state_idx, activation=ACT_NONE):
     """One token per sequence: x [N, D]; the taps of slot state_idx[n] are used and
     shifted in place.  Returns y [N, D]."""
-    x = np.asarray(x, dtype=np.float64)
+    x = _f64(x)
     N = x.shape[0]
     cu = np.arange(N + 1)
     return conv_prefill(x, weight, bias, conv_state, state_idx, cu, activation)

@@ -76,25 +76,22 @@ def test_library_scratch_entry_point_normalises_rows():
 
 def test_flag_equals_normalising_first():
     """The option on un-normalised rows gives what the kernel gives without it on the same
-    rows normalised beforehand (both within the oracle bar of each other)."""
+    rows normalised beforehand (fp32 inputs, so that normalising on the host rounds
+    nothing that matters)."""
     from kimi_delta_attention_09_gb300 import _native
-    case = _unnormalise(inputs.prefill_case([200], H=2, K=128, V=128, dtype="bf16", seed=956,
+    case = _unnormalise(inputs.prefill_case([200, 70], H=2, K=128, V=128, dtype="f32", seed=956,
                                             init_std=0.02), 957)
     o1, f1 = _run(case)
-    pre = inputs.PrefillCase(name="pre", seed=0,
-                             q=torch.from_numpy(oracle.l2_normalize(case.q)).to(torch.bfloat16),
-                             k=torch.from_numpy(oracle.l2_normalize(case.k)).to(torch.bfloat16),
-                             v=case.v, g=case.g, beta=case.beta, cu_seqlens=case.cu_seqlens,
-                             init_state=case.init_state, scale=case.scale)
-    q, k, v, g, beta = (cuda(x) for x in (pre.q, pre.k, pre.v, pre.g, pre.beta))
+    pre_q = torch.from_numpy(oracle.l2_normalize(case.q)).float()
+    pre_k = torch.from_numpy(oracle.l2_normalize(case.k)).float()
+    q, k, v, g, beta = (cuda(x) for x in (pre_q, pre_k, case.v, case.g, case.beta))
     out = torch.empty(v.shape, device="cuda")
-    fin = torch.empty(pre.N, pre.H, 128, 128, device="cuda")
-    n = _native.kda_chunk_prefill_workspace_bytes(pre.N, pre.H, 128, 128, q.dtype)
-    _native.kda_chunk_prefill_ws(q, k, v, g, beta, pre.scale, cuda(pre.init_state), cuda(pre.cu_seqlens),
-                                 out, fin, torch.zeros(n, dtype=torch.uint8, device="cuda"))
+    fin = torch.empty(case.N, case.H, 128, 128, device="cuda")
+    _native.kda_chunk_prefill(q, k, v, g, beta, case.scale, cuda(case.init_state),
+                              cuda(case.cu_seqlens), out, fin)
     torch.cuda.synchronize()
-    assert rel_err(o1, out.cpu().double().numpy()) <= TOL["bf16"]
-    assert rel_err(f1, fin.cpu().double().numpy()) <= TOL["bf16"]
+    assert rel_err(o1, out.cpu().double().numpy()) <= TOL["f32"]
+    assert rel_err(f1, fin.cpu().double().numpy()) <= TOL["f32"]
 
 
 def test_paged_prefill_normalises_rows():

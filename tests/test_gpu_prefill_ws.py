@@ -217,7 +217,7 @@ def test_workspace_must_be_device_memory_of_this_device():
     rc = _native.lib.kda_chunk_prefill_ws(
         vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), vp(g.data_ptr()),
         vp(beta.data_ptr()), case.scale, None, vp(cu.data_ptr()), vp(out.data_ptr()), None,
-        case.T, case.N, case.H, 128, 128, 1, 0, vp(host_ws.data_ptr()), n,
+        case.T, case.N, case.H, 128, 128, 1, 0, vp(host_ws.data_ptr()), n, 0,
         vp(torch.cuda.current_stream().cuda_stream))
     assert rc == _native.KDA_ERR_INVALID_ARG
     torch.cuda.synchronize()
