@@ -246,11 +246,13 @@ def prefill_block(case, times, peak_hbm, traffic_key, traffic, sample):
 
 
 def measure_e2e(args, case, bufs, stream, flush):
-    """The same prefill through the public host-to-host call (chunk_prefill_from_host):
-    pinned host inputs in, pinned host output and final state out, every H2D and D2H
-    copy inside the timed region (overlapped with the kernels piece by piece).  The
-    working buffers of the first (untimed) call are passed back, as a serving loop
-    would; the per-piece cu_seqlens they hold were copied once, outside the timing."""
+    """The same prefill through the public host-to-host call (chunk_prefill_from_host, the
+    C ABI's kda_chunk_prefill_host): pinned host inputs in, pinned host output and final
+    state out, every H2D and D2H copy inside the timed region (overlapped with the
+    kernels piece by piece inside the library).  The device buffer and pinned outputs of
+    the first (untimed) call are passed back, as a serving loop would.  Also times the
+    link alone (one H2D copy of the step's inputs, one D2H copy of its outputs, from and to
+    pinned memory), which bounds the end-to-end step from below."""
     import torch
     import kimi_delta_attention_09_gb300 as kda
     hq, hk, hv, hg, hb = (x.pin_memory() for x in (case.q, case.k, case.v, case.g, case.beta))
@@ -270,7 +272,19 @@ def measure_e2e(args, case, bufs, stream, flush):
     d2h = hout.numel() * hout.element_size() + hfin.numel() * hfin.element_size()
     n = max(3, args.steps // 2)
     times = time_steps(step, n, 3, stream, flush, sleep_cycles=0)
-    return times, h2d, d2h, n * segments   # one prefill kernel per piece
+    # the link alone
+    dev_in = torch.empty(h2d, dtype=torch.uint8, device=stream.device)
+    dev_out = torch.empty(d2h, dtype=torch.uint8, device=stream.device)
+    src = torch.empty(h2d, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(d2h, dtype=torch.uint8).pin_memory()
+    link = {}
+    for name, fn, nb in (("h2d", lambda: dev_in.copy_(src, non_blocking=True), h2d),
+                         ("d2h", lambda: dst.copy_(dev_out, non_blocking=True), d2h)):
+        lt = time_steps(fn, 5, 2, stream, flush, sleep_cycles=0)
+        link[name + "_gbs"] = round(nb / (statistics.median(lt) * 1e-3) / 1e9, 1)
+    link["floor_ms"] = round(max(h2d / link["h2d_gbs"], d2h / link["d2h_gbs"]) / 1e6, 4)
+    del dev_in, dev_out, src, dst
+    return times, h2d, d2h, n * (segments + 1), link   # per piece one prefill; one cu kernel
 
 
 def measure_decode(args, dev, stream, flush, bf16_state=False):
@@ -351,16 +365,17 @@ def run_ours(args):
             "clocks": clocks,
         })
         if args.only == "all":
-            etimes, h2d, d2h, n_e2e = measure_e2e(args, case, bufs, stream, flush)
+            etimes, h2d, d2h, n_e2e, link = measure_e2e(args, case, bufs, stream, flush)
             e_ms = statistics.mean(etimes)
             launches += n_e2e
             line["e2e"] = {"value": round(T / (e_ms * 1e-3), 1), "unit": "tokens/s",
-                           "ms_per_step": round(e_ms, 4),
-                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+                           "ms_per_step": round(e_ms, 4), "call": "kda_chunk_prefill_host",
+                           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                           "link": link, "of_link_floor": round(link["floor_ms"] / e_ms, 3)}
             if not args.no_cpu_baseline:
                 line["cpu_baseline"] = cpu_oracle_baseline(case, n_tokens=T)
         del bufs
-        if args.only == "all":
+        if args.only in ("all", "prefill"):
             from kimi_delta_attention_09_gb300 import inputs
             for key, make, tkey in (("prefill_varlen", inputs.varlen_packed, "prefill_rr_varlen_packed"),
                                     ("prefill_long", inputs.long_prefill, "prefill_rr_long_prefill")):

@@ -25,6 +25,8 @@
  *                            paged pool slot, updated in place (state slots keyed
  *                            by per-sequence indices, PR #122 block B2); its
  *                            _bf16_state form keeps the pool in bf16.
+ *   kda_chunk_prefill_host -- the prefill of a prompt held in HOST memory, outputs
+ *                            returned to host memory, the copies overlapped with it.
  *   kda_causal_conv1d_fwd / _update -- the short causal convolution in front of the
  *                            op over the packed [q|k|v] channels, its taps carried per
  *                            slot (PR #122 block B2; PR #113 commit body).
@@ -44,6 +46,8 @@
  *  * The caller owns every buffer.  The library allocates no device or host memory
  *    and synchronises nothing (except kda_chunk_prefill_status, which says so): all
  *    work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *    (kda_chunk_prefill_host also uses two copy streams and a few events of its own,
+ *    created on its first call per device and kept until exit.)
  *    Errors from the kernels themselves surface at the caller's next synchronisation.
  *  * Prefill scratch.  The tensor-core prefill (bf16 q/k/v, K = V = 128) runs one
  *    4-CTA thread-block cluster per (sequence, head); each CTA builds every fourth
@@ -83,7 +87,7 @@
 extern "C" {
 #endif
 
-#define KDA_ABI_VERSION 4
+#define KDA_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define KDA_API __attribute__((visibility("default")))
@@ -356,6 +360,50 @@ KDA_API int kda_recurrent_decode_bf16_state(const void *q, const void *k, const 
                                             int32_t num_seqs, int32_t num_slots, int32_t num_heads,
                                             int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
                                             int32_t out_dtype, int32_t flags, void *stream);
+
+/*
+ * kda_chunk_prefill_host -- kda_chunk_prefill of a prompt whose inputs are in HOST memory,
+ * with the outputs and the final states returned to host memory.  The prompt path of
+ * vllm.cpp PR #113 ("paged-incremental decode", commit body): the prompt is prefilled once
+ * with the chunked kernel and its state carried into decode.
+ *
+ * The packed token range is cut into `pieces` (1..KDA_HOST_MAX_PIECES) pieces on 64-token
+ * boundaries.  Piece s is copied host-to-device on a copy stream, prefilled on `stream`
+ * (every sequence clipped to the piece, its state carried in place from the previous
+ * piece), and its output rows are copied device-to-host on a second copy stream, so the
+ * copies of neighbouring pieces overlap the prefill.  A prefill split at any token and
+ * continued from the carried state is the unsplit prefill (up to rounding).
+ *
+ *   q, k, v, g, beta, cu_seqlens, init_state (or NULL: zeros)   HOST inputs, the layouts
+ *                    of kda_chunk_prefill; page-locked memory lets the copies run
+ *                    asynchronously (pageable memory works, with staged copies).
+ *   out, final_state (or NULL: not returned)   HOST outputs, valid once `stream` has been
+ *                    synchronised.
+ *   device_buffer    device memory of the current GPU, 256-byte aligned, at least
+ *                    kda_chunk_prefill_host_device_bytes(...) bytes, zero-filled before
+ *                    its first use.  It starts with the prefill workspace, so
+ *                    kda_chunk_prefill_status(device_buffer, stream) reports this call's
+ *                    status.  One call at a time per buffer.
+ *   flags            as for kda_chunk_prefill.
+ * Errors: KDA_ERR_INVALID_ARG (sizes, pieces, a NULL input, the buffer), KDA_ERR_ALIAS (a
+ * host output overlapping a host input or the other output), KDA_ERR_UNSUPPORTED (dtypes,
+ * head sizes); on those nothing is enqueued.  KDA_ERR_CUDA from the runtime (work already
+ * enqueued by this call then stays enqueued).
+ * The function only enqueues work; calls from several host threads are serialised while
+ * they enqueue.
+ */
+#define KDA_HOST_MAX_PIECES 16
+KDA_API size_t kda_chunk_prefill_host_device_bytes(int64_t total_tokens, int32_t num_seqs,
+                                                   int32_t num_heads, int32_t head_dim_k,
+                                                   int32_t head_dim_v, int32_t dtype,
+                                                   int32_t out_dtype, int32_t pieces);
+KDA_API int kda_chunk_prefill_host(const void *q, const void *k, const void *v, const float *g,
+                                   const float *beta, float scale, const float *init_state,
+                                   const int32_t *cu_seqlens, void *out, float *final_state,
+                                   int64_t total_tokens, int32_t num_seqs, int32_t num_heads,
+                                   int32_t head_dim_k, int32_t head_dim_v, int32_t dtype,
+                                   int32_t out_dtype, int32_t pieces, void *device_buffer,
+                                   size_t device_buffer_bytes, int32_t flags, void *stream);
 
 /* Activation of the causal convolution. */
 enum kda_conv_activation {

@@ -9,8 +9,7 @@ pointers; importing the op functions raises if the library is missing.
 """
 from __future__ import annotations
 
-__all__ = ["chunk_prefill", "chunk_prefill_paged", "chunk_prefill_from_host", "piece_bounds",
-           "piece_cu_seqlens", "recurrent_decode",
+__all__ = ["chunk_prefill", "chunk_prefill_paged", "chunk_prefill_from_host", "recurrent_decode",
            "prefill_workspace", "kda_chunk_prefill", "kda_chunk_prefill_ws",
            "kda_chunk_prefill_paged_ws", "kda_chunk_prefill_noalloc",
            "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_paged", "kda_chunk_prefill_status",
@@ -125,47 +124,24 @@ def recurrent_decode(q, k, v, g, beta, state_pool, state_idx, scale=None, out_dt
     return out
 
 
-def piece_bounds(total_tokens: int, segments: int, chunk: int = 64):
-    """Cut the packed token range [0, total_tokens) into at most ``segments`` pieces:
-    bounds[s] .. bounds[s + 1] is piece s, every inner boundary a multiple of ``chunk``,
-    the pieces as even in chunks as the count allows.  Host logic only."""
-    T = int(total_tokens)
-    nch = (T + chunk - 1) // chunk
-    segments = max(1, min(int(segments), max(nch, 1)))
-    return [chunk * ((nch * s) // segments) for s in range(segments)] + [T]
-
-
-def piece_cu_seqlens(cu_seqlens, bounds):
-    """Per piece, the cu_seqlens of every sequence clipped to the piece and counted from
-    its first token (a sequence outside the piece has an empty range), as int32 rows
-    padded to 16 bytes.  Host logic only."""
-    import torch
-    cu = torch.as_tensor(cu_seqlens).to(torch.int64)
-    N = cu.numel() - 1
-    row = (N + 1 + 3) // 4 * 4
-    cu_seg = torch.zeros(len(bounds) - 1, row, dtype=torch.int32)
-    for s_, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
-        cu_seg[s_, :N + 1] = (cu - b0).clamp(0, b1 - b0).to(torch.int32)
-    return cu_seg
-
-
 def chunk_prefill_from_host(q, k, v, g, beta, scale=None, init_state=None, cu_seqlens=None,
-                            out_dtype=None, segments: int = 4, device=None, buffers=None):
-    """Chunked prefill of HOST (pinned) inputs, returning HOST outputs.
+                            out_dtype=None, segments: int = 4, device=None, buffers=None,
+                            qk_l2norm: bool = False):
+    """Chunked prefill of HOST (pinned) inputs, returning HOST outputs, through the C ABI's
+    ``kda_chunk_prefill_host``.
 
-    The packed token range is cut into ``segments`` pieces on chunk boundaries; the
-    host-to-device copy of piece s + 1 and the device-to-host copy of the output of
-    piece s - 1 overlap the prefill of piece s (three CUDA streams).  Each piece is one
-    ``kda_chunk_prefill_ws`` call over the tokens of every sequence that fall in it, with
-    the per-sequence states carried from piece to piece in place -- a prefill split at
-    any token and continued from the carried state equals the unsplit one.
+    The library cuts the packed token range into ``segments`` pieces on chunk boundaries
+    and overlaps the host-to-device copy of piece s + 1 and the device-to-host copy of the
+    output of piece s - 1 with the prefill of piece s; the per-sequence states are carried
+    from piece to piece in place (a prefill split at any token and continued from the
+    carried state equals the unsplit one).
 
     q, k, v, g, beta, init_state, cu_seqlens are CPU tensors (pinned memory gives
     asynchronous copies).  Returns ``(out, final_state, buffers)``: pinned CPU tensors,
     valid once the current stream of ``device`` has been synchronised, and the working
-    buffers (device tensors, pinned output tensors, streams), which a later call with
-    the same shapes, cu_seqlens and segments may pass back as ``buffers``; that call
-    then allocates nothing and overwrites the returned outputs.
+    buffers (the device buffer and the pinned outputs), which a later call with the same
+    shapes and segments may pass back as ``buffers``; that call then allocates nothing and
+    overwrites the returned outputs.
     """
     import torch
     from . import _native
@@ -177,55 +153,19 @@ def chunk_prefill_from_host(q, k, v, g, beta, scale=None, init_state=None, cu_se
     if cu_seqlens is None:
         cu_seqlens = torch.tensor([0, T], dtype=torch.int32)
     N = cu_seqlens.numel() - 1
-    bounds = piece_bounds(T, segments)
-    segments = len(bounds) - 1
+    odt = out_dtype or v.dtype
     if buffers is None:
-        # per-piece cu_seqlens, rows padded to 16 bytes (the C ABI wants 16-byte aligned pointers)
-        cu_seg = piece_cu_seqlens(cu_seqlens, bounds)
+        n = _native.kda_chunk_prefill_host_device_bytes(T, N, H, K, V, q.dtype, odt, segments)
+        _native._need(n > 0, "unsupported prefill shape for kda_chunk_prefill_host")
         buffers = {
-            "q": torch.empty(q.shape, dtype=q.dtype, device=device),
-            "k": torch.empty(k.shape, dtype=k.dtype, device=device),
-            "v": torch.empty(v.shape, dtype=v.dtype, device=device),
-            "g": torch.empty(g.shape, dtype=g.dtype, device=device),
-            "beta": torch.empty(beta.shape, dtype=beta.dtype, device=device),
-            "cu": cu_seg.to(device),
-            "out": torch.empty(v.shape, dtype=out_dtype or v.dtype, device=device),
-            "state": torch.empty(N, H, K, V, dtype=torch.float32, device=device),
-            "ws": None,
-            "hout": torch.empty(v.shape, dtype=out_dtype or v.dtype).pin_memory(),
+            "dev": torch.zeros(n, dtype=torch.uint8, device=device),
+            "hout": torch.empty(v.shape, dtype=odt).pin_memory(),
             "hfin": torch.empty(N, H, K, V, dtype=torch.float32).pin_memory(),
-            "copy": torch.cuda.Stream(device), "back": torch.cuda.Stream(device),
-            "events": [torch.cuda.Event() for _ in range(2 * segments)],
         }
-        n_ws = _native.kda_chunk_prefill_workspace_bytes(N, H, K, V, q.dtype)
-        if n_ws:
-            buffers["ws"] = torch.empty(n_ws, dtype=torch.uint8, device=device)
-    d = buffers
-    hout, hfin = d["hout"], d["hfin"]
-    main = torch.cuda.current_stream(device)
-    cs, bs = d["copy"], d["back"]
-    cs.wait_stream(main)
-    bs.wait_stream(main)
-    with torch.cuda.stream(cs):
-        if init_state is None:
-            d["state"].zero_()
-        else:
-            d["state"].copy_(init_state, non_blocking=True)
-        for s, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
-            for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
-                d[name][b0:b1].copy_(t[b0:b1], non_blocking=True)
-            d["events"][s].record(cs)
-    for s, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
-        main.wait_event(d["events"][s])
-        _native.kda_chunk_prefill_ws(d["q"][b0:b1], d["k"][b0:b1], d["v"][b0:b1], d["g"][b0:b1],
-                                     d["beta"][b0:b1], scale, d["state"], d["cu"][s, :N + 1],
-                                     d["out"][b0:b1], d["state"], d["ws"], main)
-        ev = d["events"][segments + s]
-        ev.record(main)
-        bs.wait_event(ev)
-        with torch.cuda.stream(bs):
-            hout[b0:b1].copy_(d["out"][b0:b1], non_blocking=True)
-    with torch.cuda.stream(bs):
-        hfin.copy_(d["state"], non_blocking=True)
-    main.wait_stream(bs)
+    hout, hfin = buffers["hout"], buffers["hfin"]
+    with torch.cuda.device(device):
+        _native.kda_chunk_prefill_host(q, k, v, g, beta, scale, init_state, cu_seqlens.to(torch.int32),
+                                       hout, hfin, segments, buffers["dev"],
+                                       torch.cuda.current_stream(device),
+                                       _native.KDA_FLAG_QK_L2NORM if qk_l2norm else 0)
     return hout, hfin, buffers

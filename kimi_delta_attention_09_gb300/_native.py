@@ -23,14 +23,16 @@ KDA_DTYPE_BF16 = 1
 KDA_FLAG_QK_L2NORM = 1
 KDA_CONV_ACT_NONE = 0
 KDA_CONV_ACT_SILU = 1
-ABI_VERSION = 4
+ABI_VERSION = 5
 
 EXPORTED = ("kda_abi_version", "kda_status_string", "kda_last_cuda_error",
             "kda_chunk_prefill", "kda_chunk_prefill_workspace_bytes", "kda_chunk_prefill_ws",
             "kda_chunk_prefill_noalloc", "kda_chunk_prefill_paged_ws",
             "kda_chunk_prefill_paged", "kda_chunk_prefill_status", "kda_set_prefill_wait_limit",
             "kda_recurrent_decode", "kda_recurrent_decode_bf16_state", "kda_causal_conv1d_fwd",
-            "kda_causal_conv1d_update")
+            "kda_causal_conv1d_update", "kda_chunk_prefill_host_device_bytes",
+            "kda_chunk_prefill_host")
+KDA_HOST_MAX_PIECES = 16
 
 
 class KdaError(RuntimeError):
@@ -70,6 +72,12 @@ def _load() -> ctypes.CDLL:
                                                i64, i32, i32, i32, i32, i32, i32, i32, vp,
                                                ctypes.c_size_t, i32, vp]
     lib.kda_chunk_prefill_paged_ws.restype = ctypes.c_int
+    lib.kda_chunk_prefill_host_device_bytes.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32]
+    lib.kda_chunk_prefill_host_device_bytes.restype = ctypes.c_size_t
+    lib.kda_chunk_prefill_host.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, vp, vp,
+                                           i64, i32, i32, i32, i32, i32, i32, i32, vp,
+                                           ctypes.c_size_t, i32, vp]
+    lib.kda_chunk_prefill_host.restype = ctypes.c_int
     lib.kda_chunk_prefill_status.argtypes = [vp, vp]
     lib.kda_chunk_prefill_status.restype = ctypes.c_int
     lib.kda_set_prefill_wait_limit.argtypes = [ctypes.c_uint64]
@@ -203,6 +211,50 @@ def kda_chunk_prefill_ws(q, k, v, g, beta, scale, init_state, cu_seqlens, out, f
                                   T, N, H, K, V, _dtype_code(q), _dtype_code(out), _ptr(workspace),
                                   ws_bytes, int(flags), _stream_handle(stream))
     _check("kda_chunk_prefill_ws", rc)
+
+
+def kda_chunk_prefill_host_device_bytes(T: int, N: int, H: int, K: int, V: int, dtype,
+                                        out_dtype, pieces: int) -> int:
+    """Device bytes ``kda_chunk_prefill_host`` needs (0: unsupported arguments)."""
+    code = lambda d: KDA_DTYPE_BF16 if "bfloat16" in str(d) else KDA_DTYPE_F32
+    return int(lib.kda_chunk_prefill_host_device_bytes(int(T), int(N), int(H), int(K), int(V),
+                                                       code(dtype), code(out_dtype), int(pieces)))
+
+
+def kda_chunk_prefill_host(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,
+                           pieces, device_buffer, stream=None, flags=0) -> None:
+    """Enqueue ``kda_chunk_prefill_host``: q, k, v, g, beta, cu_seqlens, init_state (or None)
+    and out, final_state (or None) are contiguous CPU tensors (page-locked for asynchronous
+    copies) in the layouts of ``kda_chunk_prefill``; ``device_buffer`` is a contiguous CUDA
+    tensor of at least ``kda_chunk_prefill_host_device_bytes`` bytes, zero-filled before its
+    first use.  The outputs are valid once ``stream`` has been synchronised."""
+    T, H, K = q.shape
+    V = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("out", out),
+                    ("cu_seqlens", cu_seqlens), ("init_state", init_state),
+                    ("final_state", final_state)):
+        if t is not None:
+            _need(not t.is_cuda and t.is_contiguous(), f"{name} must be a contiguous CPU tensor")
+    _need(device_buffer.is_cuda and device_buffer.is_contiguous(),
+          "device_buffer must be a contiguous CUDA tensor")
+    _need(k.shape == q.shape and g.shape == q.shape, "q, k, g must be [T, H, K]")
+    _need(v.shape[:2] == (T, H) and out.shape == v.shape, "v, out must be [T, H, V]")
+    _need(beta.shape == (T, H), "beta must be [T, H]")
+    _need(k.dtype == q.dtype and v.dtype == q.dtype, "q, k, v must share one dtype")
+    import torch
+    _need(g.dtype == torch.float32 and beta.dtype == torch.float32, "g, beta must be fp32")
+    _need(cu_seqlens.dtype == torch.int32, "cu_seqlens must be int32")
+    for s in (init_state, final_state):
+        if s is not None:
+            _need(s.dtype == torch.float32 and tuple(s.shape) == (N, H, K, V),
+                  "states must be fp32 [N, H, K, V]")
+    nbytes = device_buffer.numel() * device_buffer.element_size()
+    rc = lib.kda_chunk_prefill_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                    _ptr(init_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+                                    T, N, H, K, V, _dtype_code(q), _dtype_code(out), int(pieces),
+                                    _ptr(device_buffer), nbytes, int(flags), _stream_handle(stream))
+    _check("kda_chunk_prefill_host", rc)
 
 
 def kda_chunk_prefill_noalloc(q, k, v, g, beta, scale, init_state, cu_seqlens, out, final_state,

@@ -200,6 +200,10 @@ int check_prefill_paged(const void *q, const void *k, const void *v, const float
 
 }  // namespace
 
+namespace kda {
+void record_cuda_error(int e) { g_last_cuda_error = e; }
+}  // namespace kda
+
 extern "C" {
 
 int kda_abi_version(void) { return KDA_ABI_VERSION; }

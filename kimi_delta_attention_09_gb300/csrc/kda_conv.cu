@@ -17,6 +17,9 @@
 // of 64 threads covers 256 channels over 128 tokens of the packed range and slides a
 // register window of the W - 1 previous inputs down its tokens, so every input row is
 // read from HBM once (plus a W - 1 row halo per tile) and every output row written once.
+// Inside a sequence the tokens go in batches of 8 whose loads are all issued before the
+// first is used: with one load in flight per thread the pass is bound by memory latency
+// at about a third of the HBM bandwidth.
 // The prompt pass reads the old taps; a second pass, ordered after it on the stream,
 // writes the new taps (a sequence's old taps may be read by any of its tiles).
 #include "kda_internal.cuh"
@@ -28,6 +31,8 @@ constexpr int kConvThreads = 64;
 constexpr int kConvCh = 4;                               // channels per thread
 constexpr int kConvTile = 128;                           // tokens per CTA
 constexpr int kConvChPerCta = kConvThreads * kConvCh;    // 256
+constexpr int kConvBatch = 8;                            // tokens whose loads fly together
+constexpr int kConvUpdThreads = 256;                     // decode step: 1024 channels per CTA
 
 __device__ __forceinline__ void load4(const float *p, float (&v)[4])
 {
@@ -61,6 +66,30 @@ template <> struct Raw4<__nv_bfloat16> { using type = uint2; };
 __device__ __forceinline__ float act(float z, int activation)
 {
     return activation == kConvActSilu ? z / (1.f + __expf(-z)) : z;
+}
+
+// the W taps of channels c..c+3 (weight [D, W] row-major: 4W contiguous floats, 16-byte
+// aligned because c is a multiple of 4 and the pointer is)
+template <int W>
+__device__ __forceinline__ void load_weights(const float *weight, const float *bias, int c,
+                                             float (&w)[W][kConvCh], float (&b)[kConvCh])
+{
+    float f[kConvCh * W];
+#pragma unroll
+    for (int v = 0; v < W; ++v) {
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(weight + (int64_t)c * W) + v);
+        f[4 * v] = x.x; f[4 * v + 1] = x.y; f[4 * v + 2] = x.z; f[4 * v + 3] = x.w;
+    }
+#pragma unroll
+    for (int i = 0; i < kConvCh; ++i)
+#pragma unroll
+        for (int j = 0; j < W; ++j) w[j][i] = f[i * W + j];
+    if (bias) {
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(bias + c));
+        b[0] = x.x; b[1] = x.y; b[2] = x.z; b[3] = x.w;
+    } else {
+        b[0] = b[1] = b[2] = b[3] = 0.f;
+    }
 }
 
 // the sequence holding token t: the largest n with cu[n] <= t (cu non-decreasing)
@@ -97,12 +126,7 @@ kda_conv_fwd_kernel(const ConvArgs a)
     Tout *out = static_cast<Tout *>(a.out);
 
     float w[W][kConvCh], bias[kConvCh];
-#pragma unroll
-    for (int i = 0; i < kConvCh; ++i) {
-        bias[i] = a.bias ? a.bias[c + i] : 0.f;
-#pragma unroll
-        for (int j = 0; j < W; ++j) w[j][i] = a.weight[(int64_t)(c + i) * W + j];
-    }
+    load_weights<W>(a.weight, a.bias, c, w, bias);
     float win[W > 1 ? W - 1 : 1][kConvCh];   // the W - 1 inputs before the current token
 
     int n = seq_of(a.cu_seqlens, a.num_seqs, t0);
@@ -124,16 +148,46 @@ kda_conv_fwd_kernel(const ConvArgs a)
         }
     };
     bool filled = false;   // the window holds the inputs before t of sequence n
-    for (int64_t t = t0; t < t1; ++t) {
+    int64_t t = t0;
+    while (t < t1) {
         while (t >= eos && n + 1 < a.num_seqs) {   // the sequence that holds t (empty ones skipped)
             ++n;
             clamp_range(T, a.cu_seqlens[n], a.cu_seqlens[n + 1], bos, eos);
             filled = false;
         }
-        if (t < bos || t >= eos) continue;   // outside every sequence: not written
+        if (t >= eos) break;                     // past the last sequence: not written
+        if (t < bos) { t = bos < t1 ? bos : t1; continue; }   // before it: not written
         if (!filled) {
             fill(t, tap_base<Tin>(a, n, W));
             filled = true;
+        }
+        const int64_t lim = eos < t1 ? eos : t1;
+        if (t + kConvBatch <= lim) {
+            // a batch inside the sequence: inputs t .. t + 7, window before t
+            float xv[kConvBatch][kConvCh];
+#pragma unroll
+            for (int u = 0; u < kConvBatch; ++u) load4(x + (t + u) * D + c, xv[u]);
+#pragma unroll
+            for (int u = 0; u < kConvBatch; ++u) {
+                float y[kConvCh];
+#pragma unroll
+                for (int i = 0; i < kConvCh; ++i) {
+                    float acc = bias[i];
+#pragma unroll
+                    for (int j = 0; j < W; ++j) {   // input u + j of [window | batch]
+                        const int e = u + j;
+                        acc = fmaf(w[j][i], e < W - 1 ? win[e < W - 1 ? e : 0][i] : xv[e >= W - 1 ? e - (W - 1) : 0][i], acc);
+                    }
+                    y[i] = act(acc, a.activation);
+                }
+                store4(out + (t + u) * D + c, y);
+            }
+#pragma unroll
+            for (int j = 0; j < W - 1; ++j)
+#pragma unroll
+                for (int i = 0; i < kConvCh; ++i) win[j][i] = xv[kConvBatch - (W - 1) + j][i];
+            t += kConvBatch;
+            continue;
         }
         float xv[kConvCh], y[kConvCh];
         load4(x + t * D + c, xv);
@@ -154,6 +208,7 @@ kda_conv_fwd_kernel(const ConvArgs a)
 #pragma unroll
             for (int i = 0; i < kConvCh; ++i) win[W > 1 ? W - 2 : 0][i] = xv[i];
         }
+        ++t;
     }
 }
 
@@ -187,11 +242,11 @@ kda_conv_taps_kernel(const ConvArgs a)
 // One token per sequence: output from the carried taps and the token, then the taps
 // shift by one (in place, per thread).
 template <typename Tin, typename Tout, int W>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvUpdThreads)
 kda_conv_update_kernel(const ConvArgs a)
 {
     using R = typename Raw4<Tin>::type;
-    const int c = (blockIdx.y * kConvThreads + threadIdx.x) * kConvCh;
+    const int c = (blockIdx.y * kConvUpdThreads + threadIdx.x) * kConvCh;
     const int n = blockIdx.x;
     if (c >= a.dim) return;
     const int64_t D = a.dim;
@@ -210,14 +265,16 @@ kda_conv_update_kernel(const ConvArgs a)
         }
     }
     const R xraw = *reinterpret_cast<const R *>(xp);
+    float w[W][kConvCh], bias[kConvCh];
+    load_weights<W>(a.weight, a.bias, c, w, bias);
     float xv[kConvCh], y[kConvCh];
     load4(reinterpret_cast<const Tin *>(&xraw), xv);
 #pragma unroll
     for (int i = 0; i < kConvCh; ++i) {
-        float acc = a.bias ? a.bias[c + i] : 0.f;
+        float acc = bias[i];
 #pragma unroll
-        for (int j = 0; j < W - 1; ++j) acc = fmaf(a.weight[(int64_t)(c + i) * W + j], tv[j][i], acc);
-        acc = fmaf(a.weight[(int64_t)(c + i) * W + W - 1], xv[i], acc);
+        for (int j = 0; j < W - 1; ++j) acc = fmaf(w[j][i], tv[j][i], acc);
+        acc = fmaf(w[W - 1][i], xv[i], acc);
         y[i] = act(acc, a.activation);
     }
     store4(static_cast<Tout *>(a.out) + n * D + c, y);
@@ -244,8 +301,9 @@ cudaError_t launch_fwd_w(const ConvArgs &a, cudaStream_t st)
 template <typename Tin, typename Tout, int W>
 cudaError_t launch_update_w(const ConvArgs &a, cudaStream_t st)
 {
-    const dim3 grid((unsigned)a.num_seqs, (unsigned)((a.dim + kConvChPerCta - 1) / kConvChPerCta));
-    kda_conv_update_kernel<Tin, Tout, W><<<grid, kConvThreads, 0, st>>>(a);
+    const int per_cta = kConvUpdThreads * kConvCh;
+    const dim3 grid((unsigned)a.num_seqs, (unsigned)((a.dim + per_cta - 1) / per_cta));
+    kda_conv_update_kernel<Tin, Tout, W><<<grid, kConvUpdThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 

@@ -98,6 +98,10 @@ struct ConvArgs {
 cudaError_t launch_conv_fwd(const ConvArgs &a, cudaStream_t stream);
 cudaError_t launch_conv_update(const ConvArgs &a, cudaStream_t stream);
 
+// The thread's last CUDA error as kda_last_cuda_error reports it (set by every entry point
+// that returns KDA_ERR_CUDA).
+void record_cuda_error(int e);
+
 // One-token paged decode.
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 

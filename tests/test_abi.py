@@ -52,7 +52,7 @@ def test_header_compiles_as_c(tmp_path):
 
 
 def test_status_strings(native):
-    assert native.lib.kda_abi_version() == 4
+    assert native.lib.kda_abi_version() == 5
     for code, name in [(0, "KDA_OK"), (-1, "KDA_ERR_INVALID_ARG"), (-2, "KDA_ERR_UNSUPPORTED"),
                        (-3, "KDA_ERR_ALIAS"), (-4, "KDA_ERR_CUDA"), (-5, "KDA_ERR_TIMEOUT")]:
         assert native.status_string(code) == name

@@ -219,7 +219,7 @@ def test_paged_prefill_then_paged_decode():
 
 # ------------------------------------------------------------ host-staged (pipelined) prefill
 
-@pytest.mark.parametrize("segments", [1, 3, 4])
+@pytest.mark.parametrize("segments", [1, 3, 4, 16])
 def test_prefill_from_host_matches_oracle(segments):
     """Host inputs, pieces cut on 64-token boundaries of the packed range (so sequences
     are split mid-chunk and carried across pieces), nonzero initial states."""
@@ -248,3 +248,29 @@ def test_prefill_from_host_reuses_buffers():
                                             buffers=bufs)
     torch.cuda.synchronize()
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(f1, f2)
+
+
+def test_host_entry_with_one_piece_is_the_device_prefill():
+    """kda_chunk_prefill_host with one piece runs the same kernel on the same values as
+    kda_chunk_prefill_ws on device copies: bit-identical outputs and final states."""
+    from kimi_delta_attention_09_gb300 import _native
+    case = inputs.prefill_case([1, 63, 150, 65, 230], H=2, K=128, V=128, dtype="bf16", seed=75,
+                               init_std=0.02)
+    host = [x.pin_memory() for x in (case.q, case.k, case.v, case.g, case.beta)]
+    hout = torch.empty(case.T, 2, 128, dtype=torch.float32).pin_memory()
+    hfin = torch.empty(case.N, 2, 128, 128).pin_memory()
+    n = _native.kda_chunk_prefill_host_device_bytes(case.T, case.N, 2, 128, 128, torch.bfloat16,
+                                                    torch.float32, 1)
+    dev = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    _native.kda_chunk_prefill_host(*host, case.scale, case.init_state.pin_memory(), case.cu_seqlens,
+                                   hout, hfin, 1, dev)
+    q, k, v, g, beta = (cuda(x) for x in (case.q, case.k, case.v, case.g, case.beta))
+    out = torch.empty(case.T, 2, 128, device="cuda")
+    fin = torch.empty(case.N, 2, 128, 128, device="cuda")
+    ws = torch.zeros(_native.kda_chunk_prefill_workspace_bytes(case.N, 2, 128, 128, torch.bfloat16),
+                     dtype=torch.uint8, device="cuda")
+    _native.kda_chunk_prefill_ws(q, k, v, g, beta, case.scale, cuda(case.init_state),
+                                 cuda(case.cu_seqlens), out, fin, ws)
+    torch.cuda.synchronize()
+    assert _native.kda_chunk_prefill_status(dev) == _native.KDA_OK
+    assert torch.equal(hout, out.cpu()) and torch.equal(hfin, fin.cpu())

@@ -1,12 +1,36 @@
-"""Host logic of the host-to-host prefill (chunk_prefill_from_host): how the packed token
-range is cut into pieces and how each sequence is clipped to a piece, checked on the CPU
-against brute force and, through the oracle, against the unsplit prefill."""
+"""The host-to-host prefill (kda_chunk_prefill_host): the rule by which the library cuts
+the packed token range into pieces and clips each sequence to a piece, restated here and
+checked on the CPU against brute force and, through the oracle, against the unsplit
+prefill; and the entry point's argument checks, which run before any CUDA call."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from kimi_delta_attention_09_gb300 import inputs, piece_bounds, piece_cu_seqlens
+from kimi_delta_attention_09_gb300 import inputs
+
+
+def piece_bounds(total_tokens: int, segments: int, chunk: int = 64):
+    """At most ``segments`` pieces, inner bounds on multiples of ``chunk``, the pieces as
+    even in chunks as the count allows (the library's rule)."""
+    T = int(total_tokens)
+    nch = (T + chunk - 1) // chunk
+    segments = max(1, min(int(segments), max(nch, 1)))
+    return [chunk * ((nch * s) // segments) for s in range(segments)] + [T]
+
+
+def piece_cu_seqlens(cu_seqlens, bounds):
+    """Per piece, every sequence's range clipped to the piece and counted from its first
+    token (empty outside it), int32 rows padded to 16 bytes (the library's rule)."""
+    cu = torch.as_tensor(cu_seqlens).to(torch.int64)
+    N = cu.numel() - 1
+    row = (N + 1 + 3) // 4 * 4
+    cu_seg = torch.zeros(len(bounds) - 1, row, dtype=torch.int32)
+    for s_, (b0, b1) in enumerate(zip(bounds[:-1], bounds[1:])):
+        cu_seg[s_, :N + 1] = (cu - b0).clamp(0, b1 - b0).to(torch.int32)
+    return cu_seg
 
 
 @pytest.mark.parametrize("T,segments", [(0, 4), (1, 4), (64, 4), (65, 4), (4096, 4), (4096, 7),
@@ -63,3 +87,36 @@ def test_pieces_with_carried_states_equal_the_unsplit_prefill():
         out[b0:b1] = o
     assert np.abs(out - ref_out).max() <= 1e-12 * np.abs(ref_out).max()
     assert np.abs(state - ref_fin).max() <= 1e-12 * np.abs(ref_fin).max()
+
+
+def _host_call(native, pieces=4, flags=0, device_buffer=None, nbytes=0, out=None):
+    case = inputs.prefill_case([70, 30], H=2, K=128, V=128, dtype="bf16", seed=3)
+    out = torch.empty(case.T, 2, 128, dtype=torch.float32) if out is None else out
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())
+    return native.lib.kda_chunk_prefill_host(
+        vp(case.q), vp(case.k), vp(case.v), vp(case.g), vp(case.beta), case.scale, None,
+        vp(case.cu_seqlens), vp(out), None, case.T, case.N, 2, 128, 128,
+        native.KDA_DTYPE_BF16, native.KDA_DTYPE_F32, pieces, device_buffer, nbytes, flags, None)
+
+
+def test_host_entry_rejects_bad_arguments_before_any_cuda_call():
+    from kimi_delta_attention_09_gb300 import _native as native
+    assert _host_call(native, pieces=0) == native.KDA_ERR_INVALID_ARG
+    assert _host_call(native, pieces=native.KDA_HOST_MAX_PIECES + 1) == native.KDA_ERR_INVALID_ARG
+    assert _host_call(native, flags=2) == native.KDA_ERR_INVALID_ARG
+    assert _host_call(native, device_buffer=None) == native.KDA_ERR_INVALID_ARG
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: too small
+    assert _host_call(native, device_buffer=fake, nbytes=16) == native.KDA_ERR_INVALID_ARG
+
+
+def test_host_device_bytes_cover_every_region():
+    from kimi_delta_attention_09_gb300 import _native as native
+    T, N, H = 4096, 3, 32
+    n = native.kda_chunk_prefill_host_device_bytes(T, N, H, 128, 128, torch.bfloat16, torch.float32, 4)
+    ws = native.kda_chunk_prefill_workspace_bytes(N, H, 128, 128, torch.bfloat16)
+    rows = T * H
+    least = ws + rows * 128 * 2 * 3 + rows * 128 * 4 + rows * 4 + rows * 128 * 4 + N * H * 128 * 128 * 4
+    assert least <= n <= least + 12 * 256 + 4 * 4 * (N + 4)
+    assert n % 256 == 0
+    assert native.kda_chunk_prefill_host_device_bytes(T, N, H, 96, 128, torch.bfloat16, torch.float32, 4) == 0
+    assert native.kda_chunk_prefill_host_device_bytes(T, N, H, 128, 128, torch.bfloat16, torch.float32, 0) == 0
