@@ -17,9 +17,9 @@
 // of 64 threads covers 256 channels over 128 tokens of the packed range and slides a
 // register window of the W - 1 previous inputs down its tokens, so every input row is
 // read from HBM once (plus a W - 1 row halo per tile) and every output row written once.
-// Inside a sequence the tokens go in batches of 8 whose loads are all issued before the
-// first is used: with one load in flight per thread the pass is bound by memory latency
-// at about a third of the HBM bandwidth.
+// Inside a sequence the tokens go in batches (8 rows of bf16, 4 of fp32) whose loads are
+// all issued before the first is used: with one load in flight per thread the pass is
+// bound by memory latency at about a third of the HBM bandwidth.
 // The prompt pass reads the old taps; a second pass, ordered after it on the stream,
 // writes the new taps (a sequence's old taps may be read by any of its tiles).
 #include "kda_internal.cuh"
@@ -31,7 +31,8 @@ constexpr int kConvThreads = 64;
 constexpr int kConvCh = 4;                               // channels per thread
 constexpr int kConvTile = 128;                           // tokens per CTA
 constexpr int kConvChPerCta = kConvThreads * kConvCh;    // 256
-constexpr int kConvBatch = 8;                            // tokens whose loads fly together
+// tokens whose loads fly together: 64 bytes per thread (8 bf16 rows, 4 fp32 rows)
+template <typename Tin> constexpr int conv_batch() { return sizeof(Tin) == 2 ? 8 : 4; }
 constexpr int kConvUpdThreads = 256;                     // decode step: 1024 channels per CTA
 
 __device__ __forceinline__ void load4(const float *p, float (&v)[4])
@@ -114,7 +115,7 @@ __device__ __forceinline__ const Tin *tap_base(const ConvArgs &a, int n, int W)
 }
 
 template <typename Tin, typename Tout, int W>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, 16)
 kda_conv_fwd_kernel(const ConvArgs a)
 {
     const int c = (blockIdx.y * kConvThreads + threadIdx.x) * kConvCh;
@@ -162,30 +163,35 @@ kda_conv_fwd_kernel(const ConvArgs a)
             filled = true;
         }
         const int64_t lim = eos < t1 ? eos : t1;
+        constexpr int kConvBatch = conv_batch<Tin>();
         if (t + kConvBatch <= lim) {
-            // a batch inside the sequence: inputs t .. t + 7, window before t
-            float xv[kConvBatch][kConvCh];
+            // a batch inside the sequence: inputs t .. t + kConvBatch - 1 (loaded raw, all in
+            // flight at once), window before t; the window slides through the batch
+            using R = typename Raw4<Tin>::type;
+            R xr[kConvBatch];
 #pragma unroll
-            for (int u = 0; u < kConvBatch; ++u) load4(x + (t + u) * D + c, xv[u]);
+            for (int u = 0; u < kConvBatch; ++u) xr[u] = *reinterpret_cast<const R *>(x + (t + u) * D + c);
 #pragma unroll
             for (int u = 0; u < kConvBatch; ++u) {
-                float y[kConvCh];
+                float xv[kConvCh], y[kConvCh];
+                load4(reinterpret_cast<const Tin *>(&xr[u]), xv);
 #pragma unroll
                 for (int i = 0; i < kConvCh; ++i) {
                     float acc = bias[i];
 #pragma unroll
-                    for (int j = 0; j < W; ++j) {   // input u + j of [window | batch]
-                        const int e = u + j;
-                        acc = fmaf(w[j][i], e < W - 1 ? win[e < W - 1 ? e : 0][i] : xv[e >= W - 1 ? e - (W - 1) : 0][i], acc);
-                    }
-                    y[i] = act(acc, a.activation);
+                    for (int j = 0; j < W - 1; ++j) acc = fmaf(w[j][i], win[j][i], acc);
+                    y[i] = act(fmaf(w[W - 1][i], xv[i], acc), a.activation);
                 }
                 store4(out + (t + u) * D + c, y);
+#pragma unroll
+                for (int j = 0; j + 1 < W - 1; ++j)
+#pragma unroll
+                    for (int i = 0; i < kConvCh; ++i) win[j][i] = win[j + 1][i];
+                if (W > 1) {
+#pragma unroll
+                    for (int i = 0; i < kConvCh; ++i) win[W > 1 ? W - 2 : 0][i] = xv[i];
+                }
             }
-#pragma unroll
-            for (int j = 0; j < W - 1; ++j)
-#pragma unroll
-                for (int i = 0; i < kConvCh; ++i) win[j][i] = xv[kConvBatch - (W - 1) + j][i];
             t += kConvBatch;
             continue;
         }
