@@ -14,10 +14,13 @@ varlen workload's 12,288 [q|k|v] channels ("conv_prefill") and on one token of 2
 sequences ("conv_update").
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--only all|prefill|decode] [--decode-seqs S]
+                    [--only all|prefill|decode|conv] [--decode-seqs S] [--no-cpu-baseline]
 
 ``--only`` and ``--decode-seqs`` exist for profiling captures of one kernel on a
-smaller case; the default run measures everything.
+smaller case; the default run measures everything.  The end-to-end number ("e2e") is
+the same single-prompt prefill through the C ABI's host-to-host call
+(kda_chunk_prefill_host: pinned host buffers, every copy inside the timed region), with
+the host link timed beside it.
 
 Timing: CUDA events on the launching stream around each step, with L2 flushed
 (a 256 MiB write) between timed steps; a short device sleep is queued ahead of each
