@@ -64,9 +64,11 @@ template <typename T> struct Raw4;
 template <> struct Raw4<float> { using type = float4; };
 template <> struct Raw4<__nv_bfloat16> { using type = uint2; };
 
+// SiLU with the fast reciprocal division (a few ulp; the IEEE division made the prompt
+// pass issue-bound): z -> -inf gives z * 0 = -0, the limit
 __device__ __forceinline__ float act(float z, int activation)
 {
-    return activation == kConvActSilu ? z / (1.f + __expf(-z)) : z;
+    return activation == kConvActSilu ? __fdividef(z, 1.f + __expf(-z)) : z;
 }
 
 // the W taps of channels c..c+3 (weight [D, W] row-major: 4W contiguous floats, 16-byte

@@ -864,7 +864,9 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
     }
 }
 
-// clusters that can be resident at once (persistent grid), per device
+// clusters that can be resident at once (persistent grid), per device.  The value is a
+// property of the device and the kernel, not of a context, so the cache stays valid across
+// a device reset; threads that race on a device's first query store the same value.
 int max_clusters()
 {
     static int cached[64] = {0};
