@@ -476,7 +476,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                     const int r = 16 * pE + 8 * hb + u;
                     const float xx = gx[8 * hb + u].x + bx, xy = gx[8 * hb + u].y + by;   // G_r - m
                     amax = fmaxf(amax, fmaxf(fabsf(xx), fabsf(xy)));
-                    const float ex = exp2f(xx), ey = exp2f(xy);
+                    const float ex = ex2_approx(xx), ey = ex2_approx(xy);
                     const float ix = rcp_approx(ex), iy = rcp_approx(ey);
                     float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kq[8 * hb + u]));
                     float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qq[8 * hb + u]));

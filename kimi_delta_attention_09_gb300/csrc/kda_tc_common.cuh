@@ -131,6 +131,15 @@ __device__ __forceinline__ float rcp_approx(float x)
     return y;
 }
 
+// 2^x on the special-function unit (ex2.approx.ftz, relative error ~2^-22; results below
+// the normal range flush to zero, which the fast path's factors in [2^-8, 2^8] never are)
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int count)
 {
     asm volatile("bar.sync %0, %1;\n" :: "r"(id), "r"(count) : "memory");
