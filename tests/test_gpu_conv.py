@@ -106,9 +106,12 @@ def test_prompt_then_decode_equals_the_longer_prompt(W):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_update_matches_oracle(dtype):
+@pytest.mark.parametrize("D,W", [(520, 4), (260, 4), (2056, 3), (12, 2)])
+def test_update_matches_oracle(dtype, D, W):
+    """8 channels per thread when D is a multiple of 8 (520, 2056: more than one CTA of
+    channels), else 4 (260, 12)."""
     from kimi_delta_attention_09_gb300 import _native
-    case = inputs.conv_case([1] * 37, D=520, W=4, dtype=dtype, seed=84, slots=64)
+    case = inputs.conv_case([1] * 37, D=D, W=W, dtype=dtype, seed=84, slots=64)
     st = cuda(case.conv_state)
     out = torch.empty(case.x.shape, device="cuda")
     _native.kda_causal_conv1d_update(cuda(case.x), cuda(case.weight), cuda(case.bias), st,
