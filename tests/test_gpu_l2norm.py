@@ -142,3 +142,17 @@ def test_decode_normalises_rows(pool_dtype, dtype, K, V):
     tol = TOL[dtype_name(dc.steps[0].q)] if pool_dtype == "f32" else 2.0 ** -6
     used = dc.state_idx.long().numpy()
     assert rel_err(pool.float().cpu().numpy()[used], ref_pool[used]) <= tol
+
+
+def test_host_entry_normalises_rows():
+    """kda_chunk_prefill_host passes the option to every piece's prefill."""
+    import kimi_delta_attention_09_gb300 as kda
+    case = _unnormalise(inputs.prefill_case([1, 63, 150, 65, 230], H=2, K=128, V=128, dtype="bf16",
+                                            seed=958, init_std=0.02), 959)
+    pin = [x.pin_memory() for x in (case.q, case.k, case.v, case.g, case.beta)]
+    out, fin, _ = kda.chunk_prefill_from_host(*pin, case.scale, case.init_state.pin_memory(),
+                                              case.cu_seqlens, out_dtype=torch.float32, segments=3,
+                                              qk_l2norm=True)
+    torch.cuda.synchronize()
+    ref_out, ref_fin = _oracle(case)
+    assert rel_err(out, ref_out) <= TOL["bf16"] and rel_err(fin, ref_fin) <= TOL["bf16"]
