@@ -118,7 +118,7 @@ __device__ bool mbar_drain(uint32_t mbar, uint32_t parity)
 
 // mbarriers
 struct Bar { enum { slot_full = 0, slot_free = 2, a = slot_free + kRing, s1 = a + 1, s3 = s1 + 1,
-                    count = s3 + 1 }; };
+                    raw = s3 + 1, count = raw + 1 }; };
 
 // Shared memory map (byte offsets)
 struct Smem {
@@ -127,12 +127,13 @@ struct Smem {
     static constexpr int ht = 2 * slot_bytes;                // SW128 (2^m h)^T f16 32 x 128
     static constexpr int xs = ht;                            // f16 beta X [64][LDX] once S1 is done
     static constexpr int dt = ht + VT * KD * 2;              // SW128 D^T f16 32 x 64
-    static constexpr int st_aop = dt + VT * C * 2;           // builder: SW128 [a_k; a_q]
-    static constexpr int st_bk = st_aop + 2 * C * KD * 2;    // builder: SW128 b 64 x 128
+    static constexpr int st_aop = dt + VT * C * 2;           // builder: SW128 [a_k; a_q]; until P2
+                                                             // the chunk's raw g tile (TMA)
+    static constexpr int st_bk = st_aop + 2 * C * KD * 2;    // builder: SW128 b 64 x 128; until P2
+                                                             // the chunk's raw k tile (TMA)
     static constexpr int tm = st_bk;                         // builder: f16 T [64][LD64] (b is dead)
-    static constexpr int tot = st_bk;                        // builder: f32 [4][128] group sums
-    static constexpr int first = st_bk + 4 * KD * 4;         // builder: f32 [128] G of row 0
-    static constexpr int st_tw = st_bk + C * KD * 2;         // builder: SW128 T 64 x 64 (record ta rows 0..63)
+    static constexpr int st_tw = st_bk + C * KD * 2;         // builder: SW128 T 64 x 64 (record ta rows 0..63);
+                                                             // with st_akk, until P2 the raw q tile (TMA)
     static constexpr int st_akk = st_tw + C * C * 2;         // builder: SW128 A_kk 64 x 64
     static constexpr int st_vec = st_akk + C * C * 2;        // builder: beta, dec, pm (record layout)
     static constexpr int st_kht = st_tw;                     // builder: SW128 K^^T 128 x 64 over T and
@@ -145,13 +146,17 @@ struct Smem {
     static constexpr int flag = tmem + 4;
     static constexpr int nred = (flag + 4 + 15) / 16 * 16;  // builder: f32 [8 warps][32] row |x|^2 sums
     static constexpr int nscl = nred + 8 * 32 * 4;           // builder: f32 [4][q 16 | k 16] 1/|x| per row
-    static constexpr int total = nscl + 4 * 32 * 4;
+    static constexpr int tot = nscl + 4 * 32 * 4;            // builder: f32 [4][128] group sums
+    static constexpr int first = tot + 4 * KD * 4;           // builder: f32 [128] G of row 0
+    static constexpr int total = first + KD * 4;
 };
 static_assert(Smem::total <= 232448, "shared memory budget");
 static_assert(Smem::slot_bytes % 1024 == 0 && Smem::ht % 1024 == 0 && Smem::dt % 1024 == 0 &&
               Smem::st_aop % 1024 == 0 && Smem::st_bk % 1024 == 0 && Smem::st_tw % 1024 == 0 &&
               Smem::st_akk % 1024 == 0, "SW128 tiles need 1024-byte alignment");
-static_assert(C * LD64 * 2 <= C * KD * 2 && Smem::first + KD * 4 <= Smem::st_tw, "b-space aliases");
+static_assert(C * LD64 * 2 <= C * KD * 2, "the padded T fits in the b space");
+static_assert(Smem::st_akk == Smem::st_tw + C * C * 2 && 2 * C * C * 2 == C * KD * 2,
+              "the raw q tile spans the T and A_kk staging");
 static_assert(C * LDX * 2 <= VT * KD * 2, "beta X fits in the h^T space");
 
 struct RrMaps {
@@ -353,9 +358,6 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
         float *nred = reinterpret_cast<float *>(sm + Smem::nred);
         float *nscl = reinterpret_cast<float *>(sm + Smem::nscl);
         constexpr bool l2 = kL2;   // in-kernel L2 normalisation of the q and k rows
-        const float *gin = a.g;
-        const __nv_bfloat16 *qin = static_cast<const __nv_bfloat16 *>(a.q);
-        const __nv_bfloat16 *kin = static_cast<const __nv_bfloat16 *>(a.k);
         uint32_t a_parity = 0;
 
         // q, k, g tiles of chunk `ahead` chunks after the cursor's, prefetched into L2 (only
@@ -372,9 +374,34 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                 if (maps.beta_map) tma_prefetch_2d(&maps.beta, hh & ~3, z);
             }
         };
+        // The raw g, k and q tiles (64 tokens x 128 channels; g fp32, k and q bf16) of the
+        // chunk `ahead` chunks after the cursor's, by TMA into staging areas that are free
+        // from the end of one record until P2 of the next (g: [a_k; a_q]; k: b; q: T and
+        // A_kk), completing on one barrier: the builder's P1 then reads shared memory only,
+        // and the loads of its next chunk run while it finishes this one (thread 0 only)
+        uint32_t raw_parity = 0;
+        bool raw_pending = false;
+        auto load_raw = [&](const Cursor &from, int ahead) {
+            Cursor c = from;
+            bool ok = true;
+            for (int i = 0; i < ahead && ok; ++i) ok = cursor_next(c, a, G);
+            if (ok) {
+                const int hh = (int)(c.w % H), z = (int)c.t0;
+                const uint32_t mb = bar(Bar::raw);
+                fence_proxy_async_smem();   // earlier generic accesses of the staging come first
+                mbar_arrive_expect_tx(mb, C * KD * (4 + 2 + 2));
+                tma_load_3d(smem_u32(sm + Smem::st_aop), &maps.g, 0, hh, z, mb);
+                tma_load_3d(smem_u32(sm + Smem::st_bk), &maps.k, 0, hh, z, mb);
+                tma_load_3d(smem_u32(sm + Smem::st_tw), &maps.q, 0, hh, z, mb);
+            }
+            raw_pending = ok;
+        };
         Cursor pc;
         bool have = cursor_seek(pc, a, cid, G);
-        if (gtid == 0 && have) prefetch(pc, rank);
+        if (gtid == 0 && have) {
+            prefetch(pc, rank);
+            load_raw(pc, rank);
+        }
         for (int64_t ci = 0; have; ++ci, have = cursor_next(pc, a, G)) {
             if ((int)(ci % kRanks) != rank) continue;
             if (gtid == 0) prefetch(pc, kRanks);
@@ -397,16 +424,27 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
 
             // ---------------- P1: gate cumsum in exp2 space; thread = (channel pair, 16-row group E)
             const int pcp = gtid & 63, pE = gtid >> 6, pc0 = 2 * pcp;
-            // this thread's 16 rows of g, k and q (channels pc0, pc0 + 1): all loads in flight at once
+            // this thread's 16 rows of g, k and q (channels pc0, pc0 + 1) from the raw tiles
+            // (rows past the sequence's end read as zero)
+            if (wait_t(bar(Bar::raw), raw_parity, wt)) {
+                raw_parity ^= 1u;
+                if (gtid == 0) raw_pending = false;
+            } else {
+                failed = true;
+            }
             float2 gx[16];
             uint32_t kq[16], qq[16];   // bf16 pairs
+            {
+                const float *gsm = reinterpret_cast<const float *>(sm + Smem::st_aop);
+                const uint32_t *ksm = reinterpret_cast<const uint32_t *>(sm + Smem::st_bk);
+                const uint32_t *qsm = reinterpret_cast<const uint32_t *>(sm + Smem::st_tw);
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int r = 16 * pE + u;
-                const int64_t off = ((t0 + r) * H + h) * KD + pc0;
-                gx[u] = r < len ? __ldg(reinterpret_cast<const float2 *>(gin + off)) : make_float2(0.f, 0.f);
-                kq[u] = r < len ? __ldg(reinterpret_cast<const unsigned int *>(kin + off)) : 0u;
-                qq[u] = r < len ? __ldg(reinterpret_cast<const unsigned int *>(qin + off)) : 0u;
+                for (int u = 0; u < 16; ++u) {
+                    const int r = 16 * pE + u;
+                    gx[u] = r < len ? *reinterpret_cast<const float2 *>(gsm + r * KD + pc0) : make_float2(0.f, 0.f);
+                    kq[u] = r < len ? ksm[(r * KD + pc0) >> 1] : 0u;
+                    qq[u] = r < len ? qsm[(r * KD + pc0) >> 1] : 0u;
+                }
             }
 #pragma unroll
             for (int u = 0; u < 16; ++u) gx[u] = make_float2(gx[u].x * kLog2e, gx[u].y * kLog2e);
@@ -600,9 +638,11 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                                        bar(Bar::slot_full + (int)(ci & 1)), (uint16_t)((1u << kRanks) - 1));
                 else
                     failed = true;
+                load_raw(pc, kRanks);   // the raw tiles of this builder's next chunk
             }
         }
         if (failed) mbar_drain(bar(Bar::a), a_parity);   // an MMA still in flight
+        if (raw_pending) mbar_drain(bar(Bar::raw), raw_parity);   // raw tiles still in flight
     } else {
         // =====================================================================
         // State-step group (warps 0..7): the chunks of every work item of this cluster
