@@ -404,7 +404,6 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
         }
         for (int64_t ci = 0; have; ++ci, have = cursor_next(pc, a, G)) {
             if ((int)(ci % kRanks) != rank) continue;
-            if (gtid == 0) prefetch(pc, kRanks);
             const int64_t t0 = pc.t0;
             const int len = (int)((pc.eos - t0) < C ? (pc.eos - t0) : C);
             const int h = (int)(pc.w % H);
@@ -545,6 +544,10 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
             fence_proxy_async_smem();   // the operands are read by tcgen05 and the bulk copy
             named_bar_sync(kBarBuild, kGroup);
             const bool exact_path = *flag != 0;
+            // the next own chunk's tiles into L2 while the A MMA runs (issued here, off thread
+            // 0's path: at the end of a record its TMA queue holds the record's copies); the
+            // raw-tile loads of that chunk, at the end of this record, then find them there
+            if (gtid == 32) prefetch(pc, kRanks);
             unsigned char *aqk_g = rec + Rec::ta + C * C * 2;   // rows 64..127 of [T; A_qk]
 
             if (!exact_path) {
