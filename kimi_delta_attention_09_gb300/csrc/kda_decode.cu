@@ -169,10 +169,12 @@ kda_decode_kernel(DecodeArgs a)
 constexpr int kDecCols16 = 64;   // V columns per CTA on a bf16 pool
 
 // The same step on a bf16 pool: thread t owns columns [8 (t % 8), +8) of the CTA's
-// 64 on rows t / 8 + 16 j; the state is widened to fp32 on load and rounded to
-// nearest-even bf16 on store.
+// 64 on rows t / 8 + 16 j; the state is widened to fp32 where it is used and rounded to
+// nearest-even bf16 on store.  The CTA's 16 KB slice of the slot comes in by cp.async into
+// shared memory (each thread reads back only its own rows): the loads in flight then do
+// not hold registers, and 8 CTAs fit on an SM instead of 5.
 template <typename Tin, typename Tout, int K, int V, bool kL2>
-__global__ void __launch_bounds__(kDecThreads, 5)
+__global__ void __launch_bounds__(kDecThreads, 8)
 kda_decode_bf16_state_kernel(DecodeArgs a)
 {
     constexpr int kSlices = V / kDecCols16;
@@ -201,10 +203,13 @@ kda_decode_bf16_state_kernel(DecodeArgs a)
     const Tin *qp = static_cast<const Tin *>(a.q) + (n * H + h) * K;
     const float *gp = a.g + (n * H + h) * K;
 
-    uint4 raw[kRowsPerThread];
+    __shared__ __align__(16) uint4 stile[K][8];
 #pragma unroll
-    for (int j = 0; j < kRowsPerThread; ++j)
-        raw[j] = __ldcs(reinterpret_cast<const uint4 *>(S + (int64_t)(rg + 16 * j) * V));
+    for (int j = 0; j < kRowsPerThread; ++j) {
+        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&stile[rg + 16 * j][cg]);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" :: "r"(dst), "l"(S + (int64_t)(rg + 16 * j) * V) : "memory");
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
 
     float kr[kRowsPerThread], qr[kRowsPerThread], dr[kRowsPerThread];
 #pragma unroll
@@ -215,9 +220,11 @@ kda_decode_bf16_state_kernel(DecodeArgs a)
         dr[j] = expf(gp[c]);
     }
 
-    // the decayed row, widened again where it is needed (keeps 8 registers per row, not 16)
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");   // this thread's own rows
+    // the decayed row, widened where it is needed
     auto decayed = [&](int j, float (&x)[8]) {
-        const __nv_bfloat162 *w = reinterpret_cast<const __nv_bfloat162 *>(&raw[j]);
+        const uint4 rw = stile[rg + 16 * j][cg];
+        const __nv_bfloat162 *w = reinterpret_cast<const __nv_bfloat162 *>(&rw);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float2 f = __bfloat1622float2(w[e]);
