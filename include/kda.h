@@ -378,7 +378,7 @@ KDA_API int kda_recurrent_decode_bf16_state(const void *q, const void *k, const 
  *                    of kda_chunk_prefill; page-locked memory lets the copies run
  *                    asynchronously (pageable memory works, with staged copies).
  *   out, final_state (or NULL: not returned)   HOST outputs, valid once `stream` has been
- *                    synchronised.
+ *                    synchronised; final_state == init_state carries the state in place.
  *   device_buffer    device memory of the current GPU, 256-byte aligned, at least
  *                    kda_chunk_prefill_host_device_bytes(...) bytes, zero-filled before
  *                    its first use.  It starts with the prefill workspace, so
@@ -386,7 +386,8 @@ KDA_API int kda_recurrent_decode_bf16_state(const void *q, const void *k, const 
  *                    status.  One call at a time per buffer.
  *   flags            as for kda_chunk_prefill.
  * Errors: KDA_ERR_INVALID_ARG (sizes, pieces, a NULL input, the buffer), KDA_ERR_ALIAS (a
- * host output overlapping a host input or the other output), KDA_ERR_UNSUPPORTED (dtypes,
+ * host output overlapping a host input or the other output, other than the in-place state
+ * carry), KDA_ERR_UNSUPPORTED (dtypes,
  * head sizes); on those nothing is enqueued.  KDA_ERR_CUDA from the runtime (work already
  * enqueued by this call then stays enqueued).
  * The function only enqueues work; calls from several host threads are serialised while

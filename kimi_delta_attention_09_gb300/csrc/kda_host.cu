@@ -172,9 +172,6 @@ int kda_chunk_prefill_host(const void *q, const void *k, const void *v, const fl
     if (flags & ~KDA_FLAG_QK_L2NORM) return KDA_ERR_INVALID_ARG;
     if (!cu_seqlens || (total_tokens > 0 && (!q || !k || !v || !g || !beta || !out)))
         return KDA_ERR_INVALID_ARG;
-    if (!device_buffer || (reinterpret_cast<uintptr_t>(device_buffer) & 255u) != 0 ||
-        device_buffer_bytes < L.total)
-        return KDA_ERR_INVALID_ARG;
     {   // the host outputs are written while later pieces' inputs are still being read
         const size_t rows = (size_t)total_tokens * num_heads;
         const size_t es = dtype == KDA_DTYPE_BF16 ? 2 : 4, eo = out_dtype == KDA_DTYPE_BF16 ? 2 : 4;
@@ -184,10 +181,18 @@ int kda_chunk_prefill_host(const void *q, const void *k, const void *v, const fl
                                 {beta, rows * 4}, {init_state, sb},
                                 {cu_seqlens, ((size_t)num_seqs + 1) * 4}};
         const HostRange ro{out, rows * head_dim_v * eo}, rf{final_state, sb};
-        for (const HostRange &r : in)
-            if (host_overlap(ro, r) || host_overlap(rf, r)) return KDA_ERR_ALIAS;
+        for (const HostRange &r : in) {
+            if (host_overlap(ro, r)) return KDA_ERR_ALIAS;
+            // final_state == init_state carries the state in place on the host: the initial
+            // state's copy-in precedes the first prefill, the final copy-out follows the last
+            const bool carry = r.p == init_state && final_state == init_state;
+            if (!carry && host_overlap(rf, r)) return KDA_ERR_ALIAS;
+        }
         if (host_overlap(ro, rf)) return KDA_ERR_ALIAS;
     }
+    if (!device_buffer || (reinterpret_cast<uintptr_t>(device_buffer) & 255u) != 0 ||
+        device_buffer_bytes < L.total)
+        return KDA_ERR_INVALID_ARG;
     int dev = -1;
     cudaPointerAttributes attr;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&attr, device_buffer) != cudaSuccess ||

@@ -274,3 +274,22 @@ def test_host_entry_with_one_piece_is_the_device_prefill():
     torch.cuda.synchronize()
     assert _native.kda_chunk_prefill_status(dev) == _native.KDA_OK
     assert torch.equal(hout, out.cpu()) and torch.equal(hfin, fin.cpu())
+
+
+def test_host_entry_carries_the_state_in_place():
+    """final_state == init_state on the host: the initial state is read before the final
+    state is written back over it."""
+    from kimi_delta_attention_09_gb300 import _native
+    case = inputs.prefill_case([1, 63, 150, 65, 230], H=2, K=128, V=128, dtype="bf16", seed=76,
+                               init_std=0.02)
+    host = [x.pin_memory() for x in (case.q, case.k, case.v, case.g, case.beta)]
+    state = case.init_state.clone().pin_memory()
+    hout = torch.empty(case.T, 2, 128, dtype=torch.float32).pin_memory()
+    n = _native.kda_chunk_prefill_host_device_bytes(case.T, case.N, 2, 128, 128, torch.bfloat16,
+                                                    torch.float32, 3)
+    dev = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    _native.kda_chunk_prefill_host(*host, case.scale, state, case.cu_seqlens, hout, state, 3, dev)
+    torch.cuda.synchronize()
+    ref_out, ref_fin = oracle_prefill(case)
+    assert rel_err(hout, ref_out) <= TOL["bf16"]
+    assert rel_err(state, ref_fin) <= TOL["bf16"]

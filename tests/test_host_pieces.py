@@ -120,3 +120,26 @@ def test_host_device_bytes_cover_every_region():
     assert n % 256 == 0
     assert native.kda_chunk_prefill_host_device_bytes(T, N, H, 96, 128, torch.bfloat16, torch.float32, 4) == 0
     assert native.kda_chunk_prefill_host_device_bytes(T, N, H, 128, 128, torch.bfloat16, torch.float32, 0) == 0
+
+
+def test_host_entry_alias_rules():
+    """A host output overlapping an input is rejected before any CUDA call; the final state
+    may be the initial state's own buffer (the in-place carry), as on the device."""
+    from kimi_delta_attention_09_gb300 import _native as native
+    case = inputs.prefill_case([70, 30], H=2, K=128, V=128, dtype="bf16", seed=3, init_std=0.02)
+    vp = lambda t: ctypes.c_void_p(t.data_ptr())
+    state = case.init_state.clone()
+    out = torch.empty(case.T, 2, 128, dtype=torch.float32)
+
+    def call(out_t, init_t, fin_t):
+        return native.lib.kda_chunk_prefill_host(
+            vp(case.q), vp(case.k), vp(case.v), vp(case.g), vp(case.beta), case.scale,
+            None if init_t is None else vp(init_t), vp(case.cu_seqlens), vp(out_t),
+            None if fin_t is None else vp(fin_t), case.T, case.N, 2, 128, 128,
+            native.KDA_DTYPE_BF16, native.KDA_DTYPE_F32, 4, None, 0, 0, None)
+
+    # out over q: alias; final over q: alias
+    assert call(case.q, None, None) == native.KDA_ERR_ALIAS
+    assert call(out, None, case.q.view(torch.float32)) == native.KDA_ERR_ALIAS
+    # the in-place carry passes the alias rules and stops at the (missing) device buffer
+    assert call(out, state, state) == native.KDA_ERR_INVALID_ARG
