@@ -641,7 +641,7 @@ kda_prefill_rr_kernel(const PrefillArgs a, const __grid_constant__ RrMaps maps,
                                        bar(Bar::slot_full + (int)(ci & 1)), (uint16_t)((1u << kRanks) - 1));
                 else
                     failed = true;
-                load_raw(pc, kRanks);   // the raw tiles of this builder's next chunk
+                if (!failed) load_raw(pc, kRanks);   // the raw tiles of this builder's next chunk
             }
         }
         if (failed) mbar_drain(bar(Bar::a), a_parity);   // an MMA still in flight
